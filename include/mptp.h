@@ -1,0 +1,173 @@
+/*
+ * libmptp: the hot path of Megatron-LM intra-layer (tensor) model parallelism
+ * on one GB300 (sm_103a) GPU.
+ *
+ * Two computations, both from "Megatron-LM: Training Multi-Billion Parameter
+ * Language Models Using Model Parallelism" (paper-graph-ui summary), section 3.4
+ * "Detailed, Sentence-Based Technical Breakdown", and from "Tensor and pipeline
+ * parallelism, and choosing a layout" (ML Systems lesson 9), section 3,
+ * Proposition (Megatron MLP split):
+ *
+ *   1. The partitioned MLP block Z = GeLU(X A) B with A split by columns and B by
+ *      rows into t shards. The t shards live in one device's memory; the sum of
+ *      the shard partials (the page's g all-reduce) and the sum of the shards'
+ *      input gradients (the f all-reduce) are done inside the GEMM K-loop, which
+ *      visits the shards in ascending order and accumulates in tensor memory.
+ *   2. The vocab-parallel output GEMM fused with softmax cross-entropy: each
+ *      vocabulary partition reduces its logits to a per-token (max, sum-exp,
+ *      target-logit) triple; logits never reach global memory; a combine kernel
+ *      turns the triples into the per-token loss.
+ *
+ * Conventions for every entry point
+ *   - All matrices are bf16 (raw bits in mp_bf16), row-major and contiguous,
+ *     except targets (int32), loss (fp32) and workspaces (opaque bytes).
+ *   - All pointers are DEVICE pointers, 16-byte aligned. The caller allocates,
+ *     owns and frees every buffer; the library keeps no device memory between
+ *     calls and never allocates.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls only enqueue work on it and return; nothing synchronises the host.
+ *   - Argument and shape errors are reported synchronously, before any launch
+ *     (nothing is enqueued). A failed launch returns MP_ERR_CUDA.
+ *   - `d_status` (nullable, device memory, one uint32): conditions found on the
+ *     device (MP_DEV_* bits) are OR-ed into it. The caller zeroes it before the
+ *     call and reads it after synchronising the stream. With NULL they are not
+ *     reported (outputs are still written as documented).
+ *   - Every wait inside a kernel is bounded (default 2 s, environment variable
+ *     MPTP_WAIT_BUDGET_NS overrides); when a bound runs out the kernel sets
+ *     MP_DEV_TIMEOUT, lets its own copies and MMAs in flight finish, frees its
+ *     tensor memory and returns. Outputs are then undefined.
+ *   - Outputs are overwritten, never accumulated into. T = 0 is a valid no-op.
+ *   - Results are deterministic: no atomics in any reduction, fixed order.
+ */
+#ifndef MPTP_H
+#define MPTP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MP_API __attribute__((visibility("default")))
+#else
+#define MP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mp_status {
+    MP_OK = 0,
+    MP_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad t */
+    MP_ERR_UNSUPPORTED_SHAPE = 2, /* a size rule below is broken */
+    MP_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned */
+    MP_ERR_NO_DEVICE = 4,         /* current device is not compute capability 10.3 */
+    MP_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed */
+    MP_ERR_TIMEOUT = 6,           /* device bit MP_DEV_TIMEOUT was found (see mp_status_from_device) */
+    MP_ERR_TARGET_RANGE = 7,      /* device bit MP_DEV_TARGET_RANGE was found */
+    MP_ERR_WORKSPACE = 8          /* workspace too small */
+} mp_status;
+
+typedef uint16_t mp_bf16; /* raw bfloat16 bits */
+
+/* Bits OR-ed into *d_status by the kernels. */
+#define MP_DEV_TIMEOUT 0x1u
+#define MP_DEV_TARGET_RANGE 0x2u
+
+/*
+ * Forward of the sharded MLP block.
+ *   Column-parallel GEMM + GeLU (section 3.4 "Column-Parallel GEMM for the First
+ *   MLP Layer"; Proposition steps 1-2): U = X A, Y = GeLU(U), exact erf form
+ *   GeLU(u) = u (1 + erf(u / sqrt 2)) / 2, computed in fp32 from the fp32
+ *   accumulator; all t column shards A_i = A[:, i f/t : (i+1) f/t] in one launch.
+ *   Row-parallel GEMM + in-kernel g (section 3.4 "Row-Parallel GEMM for the
+ *   Second MLP Layer"; Proposition step 3): Z = sum_i Y_i B_i, shards visited in
+ *   ascending order, fp32 accumulation in tensor memory, one bf16 store.
+ *
+ *   X [T, h], A [h, f], B [f, h]            inputs
+ *   Z [T, h]                                 output
+ *   Y [T, f]                                 output (required): GeLU(U), bf16; read
+ *                                            by the row-parallel GEMM and by mp_mlp_bwd
+ *   U_save [T, f] or NULL                    output: U = X A rounded to bf16; needed
+ *                                            by mp_mlp_bwd
+ *   Size rules: T >= 0; h % 64 == 0; f % t == 0; (f / t) % 64 == 0; t >= 1.
+ */
+MP_API mp_status mp_mlp_fwd(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B,
+                     mp_bf16* Z, mp_bf16* Y, mp_bf16* U_save,
+                     int T, int h, int f, int t,
+                     uint32_t* d_status, void* stream);
+
+/*
+ * Backward of the sharded MLP block (Proposition steps 4-5), G = dZ:
+ *   dU = (G B^T) * GeLU'(U), GeLU'(u) = Phi(u) + u phi(u), U read from U_save;
+ *   dX = sum_i dU_i A_i^T  (the f operator's sum, fused into the K-loop, shards
+ *                           in ascending order);
+ *   dA = X^T dU  (all shards' dA_i side by side), dB = Y^T G.
+ *
+ *   X [T,h], A [h,f], B [f,h], U [T,f], Y [T,f], dZ [T,h]   inputs
+ *   dX [T,h], dA [h,f], dB [f,h]                           outputs
+ *   dU_ws [T,f]                                             workspace (caller-owned);
+ *                                                           holds dU (bf16) on return
+ *   Size rules as mp_mlp_fwd.
+ */
+MP_API mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B,
+                     const mp_bf16* U, const mp_bf16* Y, const mp_bf16* dZ,
+                     mp_bf16* dX, mp_bf16* dA, mp_bf16* dB, mp_bf16* dU_ws,
+                     int T, int h, int f, int t,
+                     uint32_t* d_status, void* stream);
+
+/*
+ * Bytes of workspace mp_vocab_ce needs: fp32 triples [P][3][T], P = the number
+ * of vocabulary partitions (the t shards, each cut into equal chunks of whole
+ * tiles for load balance). Returns 0 on invalid sizes.
+ */
+MP_API size_t mp_vocab_ce_workspace_bytes(int T, int v_pad, int t);
+
+/*
+ * Vocab-parallel output GEMM fused with softmax cross-entropy
+ * (section 3.4 "Output Embedding Parallelism and the Fused Cross-Entropy
+ * Optimization", steps 1-6).
+ *   Logits z[r, c] = X[r] . E[c] for c in [0, v_valid); padding rows
+ *   c >= v_valid ("Vocabulary padding for efficiency") are excluded.
+ *   loss[r] = M + log(S) - z[r, target[r]], M = max_c z, S = sum_c exp(z - M).
+ *
+ *   X [T, h] bf16, E [v_pad, h] bf16 (the vocabulary split into t row blocks of
+ *   v_pad / t), target [T] int32 in [0, v_valid), loss [T] fp32 output,
+ *   workspace >= mp_vocab_ce_workspace_bytes(T, v_pad, t) bytes (fp32 triples).
+ *   Size rules: h % 64 == 0; t >= 1; v_pad % (128 t) == 0; 1 <= v_valid <= v_pad.
+ *   A target outside [0, v_valid) sets MP_DEV_TARGET_RANGE and gives NaN loss for
+ *   that token; nothing is read out of bounds.
+ */
+MP_API mp_status mp_vocab_ce(const mp_bf16* X, const mp_bf16* E, const int32_t* target,
+                      float* loss, void* workspace, size_t workspace_bytes,
+                      int T, int h, int v_pad, int v_valid, int t,
+                      uint32_t* d_status, void* stream);
+
+/* First half of mp_vocab_ce: the logit GEMM whose epilogue writes the per-token,
+ * per-partition (max, sum-exp, target-logit) triples into workspace (steps 1-4). */
+MP_API mp_status mp_vocab_ce_partials(const mp_bf16* X, const mp_bf16* E, const int32_t* target,
+                               void* workspace, size_t workspace_bytes,
+                               int T, int h, int v_pad, int v_valid, int t,
+                               uint32_t* d_status, void* stream);
+
+/* Second half of mp_vocab_ce: combine the triples into loss (steps 5-6):
+ * M = max_p m_p, S = sum_p s_p exp(m_p - M), loss = M + log S - z_target. */
+MP_API mp_status mp_vocab_ce_combine(const void* workspace, size_t workspace_bytes,
+                              const int32_t* target, float* loss,
+                              int T, int v_pad, int v_valid, int t,
+                              uint32_t* d_status, void* stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+MP_API const char* mp_status_string(mp_status s);
+
+/* Map device status bits to the status code a caller should report
+ * (MP_OK when bits == 0; timeout takes precedence). */
+MP_API mp_status mp_status_from_device(uint32_t bits);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+MP_API int mp_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MPTP_H */

@@ -1,0 +1,126 @@
+// Entry points of the vocab-parallel fused output GEMM + cross-entropy
+// ("Megatron-LM: Training Multi-Billion Parameter Language Models Using Model
+// Parallelism", section 3.4, "Output Embedding Parallelism and the Fused
+// Cross-Entropy Optimization", steps 1-6).
+//
+//   K6  logits X E_p^T per (128-token block, vocabulary partition p); the
+//       epilogue keeps, per token, the running max m_p, the sum of exp(z - m_p)
+//       and the target logit, and writes the triple; logits stay on chip.
+//   K7  per token: M = max_p m_p, S = sum_p s_p exp(m_p - M),
+//       loss = M + log S - z_target (the page's two all-reduces and final step).
+#include "mptp_gemm.cuh"
+#include "mptp_internal.h"
+
+namespace mptp {
+
+__global__ void ce_combine_kernel(const float* __restrict__ ws, const int32_t* __restrict__ target,
+                                  float* __restrict__ loss, int T, int P, int chunk_cols, int v_valid,
+                                  uint32_t* status) {
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= T) return;
+    const long long stride = 3ll * T;
+    float M = -INFINITY;
+    for (int p = 0; p < P; ++p) M = fmaxf(M, ws[p * stride + r]);
+    float S = 0.0f;
+    for (int p = 0; p < P; ++p) {
+        const float sp = ws[p * stride + T + r];
+        if (sp > 0.0f) S += sp * expf(ws[p * stride + r] - M);
+    }
+    const int tg = target[r];
+    if (tg < 0 || tg >= v_valid) {
+        loss[r] = __int_as_float(0x7fc00000);
+        if (status) atomicOr(status, DEV_TARGET_RANGE);
+        return;
+    }
+    const float z = ws[(tg / chunk_cols) * stride + 2ll * T + r];
+    loss[r] = M + logf(S) - z;
+}
+
+static mp_status check_ce_shape(int T, int h, int v_pad, int v_valid, int t) {
+    if (T < 0 || h <= 0 || v_pad <= 0 || t < 1 || v_valid < 1) return MP_ERR_INVALID_ARG;
+    if (h % 64 != 0 || v_pad % (128 * t) != 0 || v_valid > v_pad) return MP_ERR_UNSUPPORTED_SHAPE;
+    return MP_OK;
+}
+
+}  // namespace mptp
+
+using namespace mptp;
+
+extern "C" size_t mp_vocab_ce_workspace_bytes(int T, int v_pad, int t) {
+    CePlan plan;
+    if (T < 0 || !ce_plan(v_pad, t, &plan)) return 0;
+    return size_t(plan.P) * 3 * size_t(T) * sizeof(float);
+}
+
+extern "C" mp_status mp_vocab_ce_partials(const mp_bf16* X, const mp_bf16* E, const int32_t* target,
+                                          void* workspace, size_t workspace_bytes, int T, int h, int v_pad,
+                                          int v_valid, int t, uint32_t* d_status, void* stream) {
+    mp_status st = check_ce_shape(T, h, v_pad, v_valid, t);
+    if (st != MP_OK) return st;
+    if (T == 0) return MP_OK;
+    if (!X || !E || !target || !workspace) return MP_ERR_INVALID_ARG;
+    if (!aligned16(X) || !aligned16(E) || !aligned16(target) || !aligned16(workspace) ||
+        (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)))
+        return MP_ERR_MISALIGNED;
+    if (workspace_bytes < mp_vocab_ce_workspace_bytes(T, v_pad, t)) return MP_ERR_WORKSPACE;
+    int sms = 0;
+    if ((st = check_device(&sms)) != MP_OK) return st;
+    CePlan plan;
+    ce_plan(v_pad, t, &plan);
+
+    CUtensorMap tmX, tmE;
+    if (!make_tmap_bf16(&tmX, X, h, T, h, 64, BM) || !make_tmap_bf16(&tmE, E, h, v_pad, h, 64, plan.bn))
+        return MP_ERR_CUDA;
+    GemmArgs a{};
+    a.M = T;
+    a.N = v_pad;
+    a.num_m_blocks = ceil_div(T, BM);
+    a.tiles_per_unit = plan.tiles_per_unit;
+    a.num_units = a.num_m_blocks * plan.P;
+    a.kb_begin = 0;
+    a.kb_end = h / BK;
+    a.target = target;
+    a.ws = static_cast<float*>(workspace);
+    a.v_valid = v_valid;
+    a.status = d_status;
+    a.budget_ns = wait_budget_ns();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = (plan.bn == 256) ? launch_gemm_tc<256, false, false, EPI_CE>(tmX, tmE, a, sms, s)
+                                     : launch_gemm_tc<128, false, false, EPI_CE>(tmX, tmE, a, sms, s);
+    return e == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+}
+
+extern "C" mp_status mp_vocab_ce_combine(const void* workspace, size_t workspace_bytes, const int32_t* target,
+                                         float* loss, int T, int v_pad, int v_valid, int t, uint32_t* d_status,
+                                         void* stream) {
+    if (T < 0 || v_pad <= 0 || t < 1 || v_valid < 1) return MP_ERR_INVALID_ARG;
+    if (v_pad % (128 * t) != 0 || v_valid > v_pad) return MP_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MP_OK;
+    if (!workspace || !target || !loss) return MP_ERR_INVALID_ARG;
+    if (!aligned16(workspace) || !aligned16(target) || !aligned16(loss) ||
+        (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)))
+        return MP_ERR_MISALIGNED;
+    if (workspace_bytes < mp_vocab_ce_workspace_bytes(T, v_pad, t)) return MP_ERR_WORKSPACE;
+    int sms = 0;
+    mp_status st = check_device(&sms);
+    if (st != MP_OK) return st;
+    CePlan plan;
+    ce_plan(v_pad, t, &plan);
+    const int threads = 256;
+    ce_combine_kernel<<<ceil_div(T, threads), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const float*>(workspace), target, loss, T, plan.P, plan.chunk_cols, v_valid, d_status);
+    return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+}
+
+extern "C" mp_status mp_vocab_ce(const mp_bf16* X, const mp_bf16* E, const int32_t* target, float* loss,
+                                 void* workspace, size_t workspace_bytes, int T, int h, int v_pad, int v_valid,
+                                 int t, uint32_t* d_status, void* stream) {
+    mp_status st = check_ce_shape(T, h, v_pad, v_valid, t);
+    if (st != MP_OK) return st;
+    if (T == 0) return MP_OK;
+    if (!loss) return MP_ERR_INVALID_ARG;
+    if (!aligned16(loss)) return MP_ERR_MISALIGNED;
+    st = mp_vocab_ce_partials(X, E, target, workspace, workspace_bytes, T, h, v_pad, v_valid, t, d_status, stream);
+    if (st != MP_OK) return st;
+    return mp_vocab_ce_combine(workspace, workspace_bytes, target, loss, T, v_pad, v_valid, t, d_status, stream);
+}

@@ -1,0 +1,122 @@
+// Status strings, tensor-map encoding through the driver entry point, the
+// device check and the wait budget.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdlib>
+#include <mutex>
+
+#include "mptp_internal.h"
+
+namespace mptp {
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
+                    uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch_elems * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+mp_status check_device(int* num_sms) {
+    constexpr int MAXDEV = 64;
+    static std::atomic<int> cached[MAXDEV];  // 0 unknown, -1 bad, >0 SM count
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MP_ERR_NO_DEVICE;
+    }
+    if (dev >= 0 && dev < MAXDEV) {
+        const int c = cached[dev].load(std::memory_order_relaxed);
+        if (c > 0) {
+            *num_sms = c;
+            return MP_OK;
+        }
+        if (c < 0) return MP_ERR_NO_DEVICE;
+    }
+    int maj = 0, min = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&maj, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&min, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MP_ERR_NO_DEVICE;
+    }
+    const bool ok = (maj == 10 && min == 3 && sms > 0);
+    if (dev >= 0 && dev < MAXDEV) cached[dev].store(ok ? sms : -1, std::memory_order_relaxed);
+    if (!ok) return MP_ERR_NO_DEVICE;
+    *num_sms = sms;
+    return MP_OK;
+}
+
+unsigned long long wait_budget_ns() {
+    const char* s = std::getenv("MPTP_WAIT_BUDGET_NS");
+    if (s != nullptr && *s) {
+        char* end = nullptr;
+        const unsigned long long v = std::strtoull(s, &end, 10);
+        if (end != s) return v;
+    }
+    return 2000000000ull;
+}
+
+bool ce_plan(int v_pad, int t, CePlan* plan) {
+    if (t < 1 || v_pad < 128 * t || v_pad % (128 * t) != 0) return false;
+    const int vs = v_pad / t;
+    const int bn = (vs % 256 == 0) ? 256 : 128;
+    const int nb = vs / bn;
+    int tpu = nb;
+    for (int d = 4; d <= nb; ++d)
+        if (nb % d == 0) {
+            tpu = d;
+            break;
+        }
+    plan->bn = bn;
+    plan->tiles_per_unit = tpu;
+    plan->chunk_cols = tpu * bn;
+    plan->P = v_pad / plan->chunk_cols;
+    return true;
+}
+
+}  // namespace mptp
+
+extern "C" const char* mp_status_string(mp_status s) {
+    switch (s) {
+        case MP_OK: return "MP_OK";
+        case MP_ERR_INVALID_ARG: return "MP_ERR_INVALID_ARG: null pointer, negative size or bad shard count";
+        case MP_ERR_UNSUPPORTED_SHAPE: return "MP_ERR_UNSUPPORTED_SHAPE: a size rule of the entry point is broken";
+        case MP_ERR_MISALIGNED: return "MP_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+        case MP_ERR_NO_DEVICE: return "MP_ERR_NO_DEVICE: current device is not compute capability 10.3 (sm_103a)";
+        case MP_ERR_CUDA: return "MP_ERR_CUDA: a CUDA call failed";
+        case MP_ERR_TIMEOUT: return "MP_ERR_TIMEOUT: a bounded wait inside a kernel ran out";
+        case MP_ERR_TARGET_RANGE: return "MP_ERR_TARGET_RANGE: a target id is outside [0, v_valid)";
+        case MP_ERR_WORKSPACE: return "MP_ERR_WORKSPACE: workspace smaller than required";
+    }
+    return "MP_ERR_UNKNOWN";
+}
+
+extern "C" mp_status mp_status_from_device(uint32_t bits) {
+    if (bits & MP_DEV_TIMEOUT) return MP_ERR_TIMEOUT;
+    if (bits & MP_DEV_TARGET_RANGE) return MP_ERR_TARGET_RANGE;
+    return MP_OK;
+}
+
+extern "C" int mp_version(void) { return 100; }

@@ -1,0 +1,40 @@
+// Host-side helpers shared by the entry points: tensor-map encoding, device
+// checks, the wait budget, and argument validation utilities.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/mptp.h"
+
+namespace mptp {
+
+// 2-D bf16 tensor map over a row-major [outer, inner] matrix with a row pitch of
+// pitch_elems elements; box = box_inner x box_outer elements, 128-byte swizzle,
+// zero fill out of bounds. Returns false if the driver rejects it.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
+                    uint32_t box_inner, uint32_t box_outer);
+
+// MP_OK if the current device is compute capability 10.3; fills the SM count.
+mp_status check_device(int* num_sms);
+
+// Bounded-wait budget for the kernels (ns): MPTP_WAIT_BUDGET_NS, default 2 s.
+unsigned long long wait_budget_ns();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+// Cross-entropy partitioning: each of the t vocabulary shards (v_pad / t rows
+// of E) is cut into equal chunks of whole BN-wide tiles for load balance.
+struct CePlan {
+    int bn;              // 256 or 128
+    int tiles_per_unit;  // tiles per chunk
+    int chunk_cols;      // tiles_per_unit * bn
+    int P;               // v_pad / chunk_cols partitions
+};
+bool ce_plan(int v_pad, int t, CePlan* plan);
+
+}  // namespace mptp
