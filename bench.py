@@ -1,0 +1,535 @@
+"""Throughput of the tensor-parallel hot path on one GB300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+  * the sharded MLP block at the 8.3B-layer shape (T = 4096 tokens, h = 3072,
+    f = 12288, t = 8 shards): mp_mlp_fwd (column-parallel GEMM + GeLU, row-
+    parallel GEMM with the shard sum) then mp_mlp_bwd (dU with GeLU', dX with
+    the shard sum, dA, dB);
+  * the vocab-parallel fused output GEMM + cross-entropy at the 1.2B-model
+    shape (T = 8192, h = 1536, vocabulary 50,257 padded to 51,200, t = 8):
+    mp_vocab_ce_partials then mp_vocab_ce_combine.
+
+value = algorithmic FLOP of the step (12 T h f for the MLP, 2 T h v_pad for the
+logits) / device time, in TFLOP/s. Inputs are resident in HBM when the timed
+region starts; L2 is flushed (256 MiB write) between timed steps, outside the
+per-step CUDA events. `e2e` repeats the step through the same C-ABI calls with
+pinned HOST buffers, the host-to-device copies of the inputs and the
+device-to-host copies of the results inside the timed region.
+
+`--impl reference` times the float64 CPU oracle on bounded token samples of the
+same workload instead (the reference arm); `cpu_baseline` in the main line is
+the same oracle timed once on a bounded sample.
+
+Multi-GPU (torchrun, N > 1): every rank runs its own replica of the step on
+its own batch (no data-path collective); the time is the max over ranks and
+value sums the ranks' work (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "TFLOP/s and % of GB300 BF16 tensor peak: sharded MLP fwd+bwd; vocab-CE tokens/s"
+MLP = dict(T=4096, h=3072, f=12288, t=8, seed=1003)
+CE = dict(T=8192, h=1536, v_pad=51200, v_valid=50257, t=8, seed=1002)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS_PER_STEP = 8  # fwd: 2, bwd: 4, CE: 2
+KERNEL_SOURCES = ("mptp_gemm.cuh", "mptp_ptx.cuh", "mptp_ce.cu")
+
+
+def mlp_flop(w=MLP):
+    return 12.0 * w["T"] * w["h"] * w["f"]
+
+
+def ce_flop(w=CE):
+    return 2.0 * w["T"] * w["h"] * w["v_pad"]
+
+
+def step_flop():
+    return mlp_flop() + ce_flop()
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as fh:
+            d = json.load(fh)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "tensor_transformer_layer_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
+    or None when the kernel sources changed since those counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ce_logits_lse_ncu.txt")
+    try:
+        with open(path) as fh:
+            kv = dict(line.split(":", 1) for line in fh if ":" in line and not line.startswith("#"))
+    except OSError:
+        return None
+    kv = {k.strip(): v.strip() for k, v in kv.items()}
+    if kv.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------
+def physical_gpu(local_rank: int) -> str:
+    """nvidia-smi index (or UUID) of this rank's GPU, honouring CUDA_VISIBLE_DEVICES."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(
+        os.environ.get("LOCAL_RANK", "0"))
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        return summarize_clocks(out)
+
+
+def summarize_clocks(text: str):
+    rows = []
+    for r in csv.reader(io.StringIO(text)):
+        r = [x.strip() for x in r]
+        if len(r) < 9:
+            continue
+        try:
+            rows.append((float(r[1]), float(r[2]), float(r[3]), r[5], r[6], r[7], r[8]))
+        except ValueError:
+            continue
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    loaded = [x for x in rows if x[2] > 300.0] or rows  # samples drawing real power
+    mhz = sorted(x[0] for x in loaded)
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    reasons = sorted({names[i] for x in loaded for i in range(4) if x[3 + i].lower() == "active"})
+    return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": max(x[1] for x in rows), "reasons": reasons,
+            "samples": len(loaded), "power_w_max": max(x[2] for x in rows)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+class Step:
+    """Device buffers and the C-ABI calls of one step."""
+
+    def __init__(self, dev):
+        import torch
+
+        import synth
+        import tensor_transformer_layer_gb300 as mp
+        self.mp = mp
+        self.torch = torch
+        m, c = MLP, CE
+        mi = synth.mlp_inputs(m["T"], m["h"], m["f"], m["seed"])
+        ci = synth.ce_inputs(c["T"], c["h"], c["v_pad"], c["v_valid"], c["seed"])
+        self.host_in = {"X": mi["X"], "A": mi["A"], "B": mi["B"], "dZ": mi["dZ"], "Xc": ci["X"], "E": ci["E"],
+                        "target": ci["target"]}
+        self.d = {k: v.to(dev) for k, v in self.host_in.items()}
+        T, h, f = m["T"], m["h"], m["f"]
+        bf = torch.bfloat16
+        e = lambda *s, dt=bf: torch.empty(*s, dtype=dt, device=dev)
+        self.d.update(Z=e(T, h), Y=e(T, f), U=e(T, f), dX=e(T, h), dA=e(h, f), dB=e(f, h), dU=e(T, f),
+                      loss=e(c["T"], dt=torch.float32))
+        self.ws = e(mp.mp_vocab_ce_workspace_bytes(c["T"], c["v_pad"], c["t"]), dt=torch.uint8)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.out_names = ("Z", "dX", "dA", "dB", "loss")
+
+    def run(self, ev=None):
+        """One step. ev: optional dict of CUDA events to record around the CE logit kernel."""
+        mp, d = self.mp, self.d
+        t = MLP["t"]
+        mp.mp_mlp_fwd(d["X"], d["A"], d["B"], d["Z"], d["Y"], d["U"], t=t, d_status=self.status)
+        mp.mp_mlp_bwd(d["X"], d["A"], d["B"], d["U"], d["Y"], d["dZ"], d["dX"], d["dA"], d["dB"], d["dU"], t=t,
+                      d_status=self.status)
+        if ev is not None:
+            ev["ce0"].record()
+        mp.mp_vocab_ce_partials(d["Xc"], d["E"], d["target"], self.ws, v_valid=CE["v_valid"], t=CE["t"],
+                                d_status=self.status)
+        if ev is not None:
+            ev["ce1"].record()
+        mp.mp_vocab_ce_combine(self.ws, d["target"], d["loss"], v_pad=CE["v_pad"], v_valid=CE["v_valid"],
+                               t=CE["t"], d_status=self.status)
+
+    def check_status(self):
+        s = int(self.status.item())
+        if s != 0:
+            raise RuntimeError(f"device status {s}: {self.mp.status_string(self.mp.mp_status_from_device(s))}")
+
+
+def time_device(step, steps, warmup, flush):
+    import torch
+    for _ in range(warmup):
+        step.run()
+        flush.zero_()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(steps):
+        ev = {k: torch.cuda.Event(enable_timing=True) for k in ("s0", "s1", "ce0", "ce1")}
+        ev["s0"].record()
+        step.run(ev)
+        ev["s1"].record()
+        flush.zero_()
+        evs.append(ev)
+    torch.cuda.synchronize()
+    step_ms = [e["s0"].elapsed_time(e["s1"]) for e in evs]
+    ce_ms = [e["ce0"].elapsed_time(e["ce1"]) for e in evs]
+    return step_ms, ce_ms
+
+
+def time_breakdown(step, reps, flush):
+    """Per-call device times (ms, median) of the step's four C-ABI calls."""
+    import torch
+    mp, d, t = step.mp, step.d, MLP["t"]
+    calls = {
+        "mlp_fwd": lambda: mp.mp_mlp_fwd(d["X"], d["A"], d["B"], d["Z"], d["Y"], d["U"], t=t),
+        "mlp_bwd": lambda: mp.mp_mlp_bwd(d["X"], d["A"], d["B"], d["U"], d["Y"], d["dZ"], d["dX"], d["dA"],
+                                         d["dB"], d["dU"], t=t),
+        "ce_partials": lambda: mp.mp_vocab_ce_partials(d["Xc"], d["E"], d["target"], step.ws,
+                                                       v_valid=CE["v_valid"], t=CE["t"]),
+        "ce_combine": lambda: mp.mp_vocab_ce_combine(step.ws, d["target"], d["loss"], v_pad=CE["v_pad"],
+                                                     v_valid=CE["v_valid"], t=CE["t"]),
+    }
+    out = {}
+    for name, fn in calls.items():
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ts.sort()
+        out[name] = round(ts[len(ts) // 2], 4)
+    return out
+
+
+def time_e2e(step, steps, warmup):
+    """Same step through the same calls, with pinned host inputs copied in and results copied out."""
+    import torch
+    host_in = {k: v.pin_memory() for k, v in step.host_in.items()}
+    host_out = {k: torch.empty(step.d[k].shape, dtype=step.d[k].dtype).pin_memory() for k in step.out_names}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+
+    def one():
+        for k, v in host_in.items():
+            step.d[k].copy_(v, non_blocking=True)
+        step.run()
+        for k, v in host_out.items():
+            v.copy_(step.d[k], non_blocking=True)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# oracle on the host cores (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """The float64 oracle on token samples of the same workload (full weights)."""
+
+    def __init__(self, mlp_tokens: int, ce_tokens: int):
+        import synth
+        m, c = MLP, CE
+        mi = synth.mlp_inputs(m["T"], m["h"], m["f"], m["seed"])
+        ci = synth.ce_inputs(c["T"], c["h"], c["v_pad"], c["v_valid"], c["seed"])
+        f64 = synth.to_f64
+        self.X = f64(mi["X"][:mlp_tokens])
+        self.dZ = f64(mi["dZ"][:mlp_tokens])
+        self.A = f64(mi["A"])
+        self.B = f64(mi["B"])
+        self.Xc = f64(ci["X"][:ce_tokens])
+        self.E = f64(ci["E"])
+        self.tgt = ci["target"][:ce_tokens].numpy()
+        self.mlp_tokens, self.ce_tokens = mlp_tokens, ce_tokens
+
+    def flop(self):
+        return (12.0 * self.mlp_tokens * MLP["h"] * MLP["f"] + 2.0 * self.ce_tokens * CE["h"] * CE["v_pad"])
+
+    def run(self):
+        import oracle
+        oracle.mlp_fwd(self.X, self.A, self.B)
+        oracle.mlp_bwd(self.X, self.A, self.B, self.dZ)
+        oracle.ce_loss(self.Xc, self.E, self.tgt, CE["v_valid"])
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(sample: OracleSample, min_seconds: float, max_reps: int):
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        sample.run()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return sample.flop() * reps / el / 1e12, el, reps
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    sample = OracleSample(mlp_tokens=8, ce_tokens=16)
+    for _ in range(args.warmup):
+        sample.run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sample.run()
+    el = time.perf_counter() - t0
+    value = sample.flop() * args.steps / el / 1e12
+    desc = (f"float64 oracle per step on {sample.mlp_tokens} MLP tokens (full 3072x12288 weights, fwd+bwd) "
+            f"and {sample.ce_tokens} CE tokens (full 51,200x1536 embedding)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config():
+    return {
+        "workload": "sharded MLP fwd+bwd at the 8.3B-layer shape + vocab-parallel fused CE at the 1.2B shape",
+        "mlp": {"T": MLP["T"], "b": 4, "s": 1024, "h": MLP["h"], "f": MLP["f"], "t": MLP["t"]},
+        "ce": {"T": CE["T"], "b": 8, "s": 1024, "h": CE["h"], "v_pad": CE["v_pad"], "v_valid": CE["v_valid"],
+               "t": CE["t"]},
+        "flop_per_step": step_flop(),
+        "l2": "flushed between timed steps (256 MiB write outside the step events); step inputs > L2",
+        "inputs": "seeded synthetic bf16: X, dZ ~ N(0,1); A, B, E ~ N(0, 0.02); targets uniform in [0, 50257)",
+    }
+
+
+# ---------------------------------------------------------------------------
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("mptp", "reference"), default="mptp")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
+    ap.add_argument("--profile-case", choices=("none", "ce", "mlp"), default="none",
+                    help="run only a small case of one entry point a few times (for ncu), print nothing")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.profile_case == "none":
+        ap.error("--warmup must be >= 3")
+
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+
+    from tensor_transformer_layer_gb300 import build as _build
+    _build.build()
+
+    if args.profile_case != "none":
+        return profile_case(args.profile_case, dev)
+
+    step = Step(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    step.run()
+    torch.cuda.synchronize()
+    step.check_status()
+
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(physical_gpu(local_rank))
+    sampler.start()
+    step_ms, ce_ms = time_device(step, args.steps, args.warmup, flush)
+    clocks = sampler.stop()
+    torch.cuda.synchronize()
+    barrier(world)
+    step.check_status()
+
+    local_total = sum(step_ms)
+    total_ms = max_over_ranks(local_total, world, dev)
+    ms_per_step = total_ms / args.steps
+    value = world * step_flop() * args.steps / (total_ms * 1e-3) / 1e12
+
+    breakdown = time_breakdown(step, 9, flush)
+    peaks, peak_src = load_peaks()
+    ce_avg_ms = sum(ce_ms) / len(ce_ms)
+    ce_achieved = ce_flop() / (ce_avg_ms * 1e-3) / 1e12
+    traffic = profiled_traffic()
+    mlp_ms = breakdown["mlp_fwd"] + breakdown["mlp_bwd"]
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = time_e2e(step, max(3, min(args.steps, 20)), 2)
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
+        e2e = {"value": world * step_flop() / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    step.check_status()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        del step
+        torch.cuda.empty_cache()
+        sample = OracleSample(mlp_tokens=64, ce_tokens=128)
+        v, el, reps = time_oracle(sample, min_seconds=10.0, max_reps=50)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"float64 oracle, {reps} pass(es) of {sample.mlp_tokens} MLP tokens (fwd+bwd, full "
+                         f"weights) + {sample.ce_tokens} CE tokens (full embedding) in {el:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(),
+            "pct_of_measured_bf16_sustained": value / peaks["bf16_tflops_sustained"],
+            "mlp_fwd_bwd_tflops": mlp_flop() / (mlp_ms * 1e-3) / 1e12,
+            "ce_tokens_per_s": CE["T"] / ((breakdown["ce_partials"] + breakdown["ce_combine"]) * 1e-3),
+            "ce_tflops": ce_flop() / ((breakdown["ce_partials"] + breakdown["ce_combine"]) * 1e-3) / 1e12,
+            "breakdown_ms": breakdown,
+            "roofline": {"kernel": "mp_vocab_ce_partials (logit GEMM + online LSE epilogue)", "bound": "tensor",
+                         "achieved": ce_achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                         "frac": ce_achieved / peaks["bf16_tflops_sustained"],
+                         "peak_source": f"{peak_src} bf16 sustained", "traffic": traffic,
+                         "algorithmic_flop_per_launch": ce_flop(), "avg_launch_ms": ce_avg_ms},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": KERNELS_PER_STEP * (args.steps),
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def profile_case(which, dev):
+    """Small cases for ncu captures (a few GB on the device at most, inputs > L2)."""
+    import torch
+
+    import synth
+    import tensor_transformer_layer_gb300 as mp
+    if which == "ce":
+        T, h, v_pad, v_valid, t = 2048, 1536, 51200, 50257, 8
+        ci = synth.ce_inputs(T, h, v_pad, v_valid, seed=1002)
+        X, E, tgt = ci["X"].to(dev), ci["E"].to(dev), ci["target"].to(dev)
+        ws = torch.empty(mp.mp_vocab_ce_workspace_bytes(T, v_pad, t), dtype=torch.uint8, device=dev)
+        loss = torch.empty(T, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            mp.mp_vocab_ce(X, E, tgt, loss, ws, v_valid=v_valid, t=t)
+    else:
+        T, h, f, t = 1024, 3072, 12288, 8
+        mi = synth.mlp_inputs(T, h, f, seed=1003)
+        d = {k: v.to(dev) for k, v in mi.items()}
+        e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=dev)
+        Z, Y, U, dX, dA, dB, dU = e(T, h), e(T, f), e(T, f), e(T, h), e(h, f), e(f, h), e(T, f)
+        for _ in range(3):
+            mp.mp_mlp_fwd(d["X"], d["A"], d["B"], Z, Y, U, t=t)
+            mp.mp_mlp_bwd(d["X"], d["A"], d["B"], U, Y, d["dZ"], dX, dA, dB, dU, t=t)
+    torch.cuda.synchronize()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

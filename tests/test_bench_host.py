@@ -1,0 +1,79 @@
+"""Host-side logic of bench.py (CPU only): clock parsing, max over ranks with a
+2-rank gloo group, and the reference arm's JSON line."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_summarize_clocks():
+    text = ("0, 1890, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, Active\n"
+            "0, 1905, 2070, 950.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+            "0, 165, 2070, 120.0, 0x1, Not Active, Not Active, Not Active, Not Active\n"
+            "garbage line\n")
+    c = bench.summarize_clocks(text)
+    assert c["sm_max_mhz"] == 2070.0
+    assert c["samples"] == 2                      # idle sample (120 W) excluded
+    assert c["sm_mhz"] in (1890.0, 1905.0)
+    assert c["reasons"] == ["sw_power_cap"]
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    v = bench.max_over_ranks(10.0 + rank * 5.0, world, device="cpu")
+    bench.barrier(world)
+    out[rank] = v
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    ctx = mp.get_context("spawn")
+    manager = ctx.Manager()
+    out = manager.dict()
+    port = 29500 + (os.getpid() % 1000)
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0] == 15.0 and out[1] == 15.0
+
+
+def test_single_rank_identity():
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_flop_accounting():
+    assert bench.mlp_flop() == 12 * 4096 * 3072 * 12288
+    assert bench.ce_flop() == 2 * 8192 * 1536 * 51200
+    assert bench.step_flop() == bench.mlp_flop() + bench.ce_flop()
+
+
+def test_physical_gpu(monkeypatch):
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "3,5")
+    assert bench.physical_gpu(1) == "5"
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES")
+    assert bench.physical_gpu(0) == "0"
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="CPU-only check of the reference arm's line")
+def test_reference_arm_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["metric"] == bench.METRIC
