@@ -156,6 +156,31 @@ MP_API mp_status mp_vocab_ce_combine(const void* workspace, size_t workspace_byt
                               int T, int v_pad, int v_valid, int t,
                               uint32_t* d_status, void* stream);
 
+/*
+ * mp_vocab_ce for callers that cannot allocate device memory. The paper has no
+ * counterpart to this entry point; it exists for callers whose device memory is
+ * owned by another pool (a serving runtime that reserves HBM at start-up and
+ * forbids later cudaMalloc/cudaFree, which can synchronise the device; a host
+ * framework that must account for every byte), so they cannot pass a workspace.
+ *
+ * Same inputs, outputs and size rules as mp_vocab_ce, without the workspace: the
+ * triples live in a static device array of MP_CE_NOALLOC_MAX_FLOATS floats
+ * (4 MiB) that the library reserves on every GPU that loads it, until exit.
+ *   - Problems needing more than that (mp_vocab_ce_workspace_bytes(T, v_pad, t)
+ *     > 4 MiB, e.g. T > 8738 at v_pad = 51,200, t = 8) return MP_ERR_WORKSPACE
+ *     before any launch.
+ *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address with that
+ *     device current; make that first call before any stream capture.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents (nothing in it needs to start at zero). Calls whose work overlaps
+ *     on the GPU (other streams, other host threads) race on it: serialise them.
+ */
+#define MP_CE_NOALLOC_MAX_FLOATS (1024 * 1024)
+MP_API mp_status mp_vocab_ce_noalloc(const mp_bf16* X, const mp_bf16* E, const int32_t* target,
+                              float* loss, int T, int h, int v_pad, int v_valid, int t,
+                              uint32_t* d_status, void* stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 MP_API const char* mp_status_string(mp_status s);
 

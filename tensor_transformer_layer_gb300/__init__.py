@@ -31,7 +31,8 @@ STATUS_NAMES = {
 }
 # Every symbol include/mptp.h declares.
 EXPORTS = ("mp_mlp_fwd", "mp_mlp_bwd", "mp_vocab_ce_workspace_bytes", "mp_vocab_ce", "mp_vocab_ce_partials",
-           "mp_vocab_ce_combine", "mp_status_string", "mp_status_from_device", "mp_version")
+           "mp_vocab_ce_combine", "mp_status_string", "mp_status_from_device", "mp_version",
+           "mp_vocab_ce_noalloc")
 
 
 class MptpError(RuntimeError):
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
         L.mp_vocab_ce_partials.restype = _I
         L.mp_vocab_ce_combine.argtypes = [_P, ctypes.c_size_t, _P, _P, _I, _I, _I, _I, _P, _P]
         L.mp_vocab_ce_combine.restype = _I
+        L.mp_vocab_ce_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]
+        L.mp_vocab_ce_noalloc.restype = _I
         L.mp_status_string.argtypes = [_I]
         L.mp_status_string.restype = ctypes.c_char_p
         L.mp_status_from_device.argtypes = [ctypes.c_uint32]
@@ -185,6 +188,19 @@ def mp_vocab_ce_combine(workspace, target, loss, *, v_pad: int, v_valid: int, t:
         _ptr(loss, "loss", dtype=torch.float32, shape=(T,)), T, int(v_pad), int(v_valid), int(t),
         _status_ptr(d_status), _stream(stream))
     _check("mp_vocab_ce_combine", code)
+
+
+def mp_vocab_ce_noalloc(X, E, target, loss, *, v_valid: int, t: int, d_status=None, stream=None) -> None:
+    """mp_vocab_ce without a workspace argument, for callers that cannot allocate
+    device memory: the library's fixed 4 MiB static device array holds the
+    triples. Calls that overlap on the GPU race on that array."""
+    T, h = X.shape
+    v_pad = E.shape[0]
+    code = lib().mp_vocab_ce_noalloc(
+        _ptr(X, "X", shape=(T, h)), _ptr(E, "E", shape=(v_pad, h)),
+        _ptr(target, "target", dtype=torch.int32, shape=(T,)), _ptr(loss, "loss", dtype=torch.float32, shape=(T,)),
+        T, h, v_pad, int(v_valid), int(t), _status_ptr(d_status), _stream(stream))
+    _check("mp_vocab_ce_noalloc", code)
 
 
 def mp_status_from_device(bits: int) -> int:
