@@ -407,7 +407,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("mptp", "reference"), default="mptp")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
-    ap.add_argument("--profile-case", choices=("none", "ce", "mlp"), default="none",
+    ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "mlp"), default="none",
                     help="run only a small case of one entry point a few times (for ncu), print nothing")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.profile_case == "none":
@@ -505,13 +505,15 @@ def main(argv=None):
 
 
 def profile_case(which, dev):
-    """Small cases for ncu captures (a few GB on the device at most, inputs > L2)."""
+    """Cases for ncu captures: 'ce' (T=2048) and 'mlp' (the 8.3B layer, 0.7 GB) are small enough for
+    multi-pass captures (under 1 GB on the device, 0.2-0.7 ms kernels, inputs > L2); 'ce_full' is the
+    bench's CE launch, for one-pass metrics only."""
     import torch
 
     import synth
     import tensor_transformer_layer_gb300 as mp
-    if which == "ce":
-        T, h, v_pad, v_valid, t = 2048, 1536, 51200, 50257, 8
+    if which in ("ce", "ce_full"):
+        T, h, v_pad, v_valid, t = (2048 if which == "ce" else CE["T"]), 1536, 51200, 50257, 8
         ci = synth.ce_inputs(T, h, v_pad, v_valid, seed=1002)
         X, E, tgt = ci["X"].to(dev), ci["E"].to(dev), ci["target"].to(dev)
         ws = torch.empty(mp.mp_vocab_ce_workspace_bytes(T, v_pad, t), dtype=torch.uint8, device=dev)
@@ -519,8 +521,8 @@ def profile_case(which, dev):
         for _ in range(3):
             mp.mp_vocab_ce(X, E, tgt, loss, ws, v_valid=v_valid, t=t)
     else:
-        T, h, f, t = 1024, 3072, 12288, 8
-        mi = synth.mlp_inputs(T, h, f, seed=1003)
+        T, h, f, t = MLP["T"], MLP["h"], MLP["f"], MLP["t"]
+        mi = synth.mlp_inputs(T, h, f, seed=MLP["seed"])
         d = {k: v.to(dev) for k, v in mi.items()}
         e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=dev)
         Z, Y, U, dX, dA, dB, dU = e(T, h), e(T, f), e(T, f), e(T, h), e(h, f), e(f, h), e(T, f)

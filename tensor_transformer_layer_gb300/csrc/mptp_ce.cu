@@ -85,8 +85,8 @@ extern "C" mp_status mp_vocab_ce_partials(const mp_bf16* X, const mp_bf16* E, co
     a.status = d_status;
     a.budget_ns = wait_budget_ns();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = (plan.bn == 256) ? launch_gemm_tc<256, false, false, EPI_CE>(tmX, tmE, a, sms, s)
-                                     : launch_gemm_tc<128, false, false, EPI_CE>(tmX, tmE, a, sms, s);
+    cudaError_t e = (plan.bn == 256) ? launch_gemm_tc<256, false, false, EPI_CE, 4>(tmX, tmE, tmX, tmX, a, sms, s)
+                                     : launch_gemm_tc<128, false, false, EPI_CE, 4>(tmX, tmE, tmX, tmX, a, sms, s);
     return e == cudaSuccess ? MP_OK : MP_ERR_CUDA;
 }
 

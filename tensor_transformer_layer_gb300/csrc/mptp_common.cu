@@ -24,8 +24,8 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
-                    uint32_t box_inner, uint32_t box_outer) {
+static bool make_tmap_bf16_sw(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer,
+                              uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     cuuint64_t dims[2] = {inner, outer};
@@ -33,9 +33,18 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
+}
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
+                    uint32_t box_inner, uint32_t box_outer) {
+    return make_tmap_bf16_sw(map, base, inner, outer, pitch_elems, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool make_tmap_bf16_out(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems) {
+    return make_tmap_bf16_sw(map, base, inner, outer, pitch_elems, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 mp_status check_device(int* num_sms) {

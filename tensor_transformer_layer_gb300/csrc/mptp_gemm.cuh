@@ -2,16 +2,19 @@
 //
 //   C[M, N] = sum_k  A(m, k) * B(k, n),   bf16 inputs, fp32 accumulation in TMEM.
 //
-// One CTA per SM (grid = min(work units, SMs)); 192 threads:
+// One CTA per SM (grid = min(work units, SMs)); 64 + 32*NE threads:
 //   warp 0      TMA producer (one elected lane): 128x64 A tile + BNx64 B tile per
 //               stage into a STAGES-deep shared-memory ring, 128-byte swizzle.
 //   warp 1      TMEM allocator (whole warp) and MMA issuer (one lane): 4 x
 //               tcgen05.mma (M=128, N=BN, K=16) per stage into one of two TMEM
 //               accumulators (double buffer: 2*BN fp32 columns).
-//   warps 2..5  epilogue: tcgen05.ld 32 rows x 32 columns per warp (TMEM lane
-//               quarter = warp % 4, thread = output row), fused math, bf16 store
-//               or cross-entropy partials. Runs while the MMA fills the other
-//               accumulator.
+//   warps 2..   NE epilogue warps (4 or 8): tcgen05.ld 32 rows x 32 columns per
+//               warp (TMEM lane quarter = warp % 4, thread = output row; with 8
+//               warps two warps share a quarter and split the columns), fused
+//               math, then bf16 rows staged in a 64-byte-swizzled shared buffer
+//               and written by TMA stores (32x32 boxes), or cross-entropy
+//               partials. Runs while the MMA fills the other accumulator; the
+//               accumulator is released as soon as its last columns are read.
 //
 // A work unit is one 128-row block and `tiles_per_unit` consecutive BN-wide
 // column tiles (1 for plain GEMMs; several for the cross-entropy, whose epilogue
@@ -38,8 +41,7 @@ namespace mptp {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int UMMA_K = 16;
-constexpr int NUM_THREADS = 192;
-constexpr int NUM_EPI_WARPS = 4;
+constexpr int STG_BYTES_PER_WARP = 2 * 2048;  // two 32x32 bf16 staging boxes
 constexpr uint32_t DEV_TIMEOUT = 0x1u;
 constexpr uint32_t DEV_TARGET_RANGE = 0x2u;
 constexpr unsigned long long DRAIN_BUDGET_NS = 1000000000ull;  // 1 s
@@ -55,6 +57,7 @@ struct GemmArgs {
     int M, N;                 // output extent (masking of the ragged tails)
     int num_m_blocks;         // ceil(M / BM)
     int num_units;            // num_m_blocks * unit columns
+    int n_fastest;            // unit order: 0 = row blocks fastest, 1 = column units fastest
     int tiles_per_unit;       // BN-wide column tiles per unit
     int kb_begin, kb_end;     // K blocks (of BK) to accumulate, ascending
     __nv_bfloat16* out0;
@@ -71,16 +74,22 @@ struct GemmArgs {
     unsigned long long budget_ns;
 };
 
-template <int BN_>
+template <int BN_, int EPI, int NE_>
 struct GemmCfg {
     static constexpr int BN = BN_;
+    static constexpr int NE = NE_;
+    static constexpr int NUM_THREADS = 64 + 32 * NE;
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int STAGES = (BN == 256) ? 4 : 6;
     static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr int STG_BYTES = (EPI == EPI_CE) ? 0 : NE * STG_BYTES_PER_WARP;
     static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem full x2, tmem empty x2, drain
-    static constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + 8 * NUM_BARS + 16;
+    static constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + STG_BYTES + 8 * NUM_BARS + 16;
+    static_assert(SMEM_BYTES <= 232448, "shared memory per block");
+    static_assert(NE == 4 || NE == 8, "4 or 8 epilogue warps");
+    static_assert(EPI != EPI_CE || NE == 4, "cross-entropy epilogue keeps one thread per row");
 };
 
 struct Ctl {
@@ -126,36 +135,92 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ float gelu_f(float u) {
-    return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f));
+// Standard normal CDF and density from one exponential, with erf taken from the
+// rational approximation of Abramowitz & Stegun, Handbook of Mathematical
+// Functions, eq. 7.1.26 (|error of erf| <= 1.5e-7 for x >= 0):
+//   erf(x) = 1 - (a1 s + a2 s^2 + a3 s^3 + a4 s^4 + a5 s^5) e^{-x^2},  s = 1 / (1 + p x).
+// With x = |u| / sqrt 2 and q = (1 - erf(x)) / 2, Phi(u) = 1 - q for u >= 0 and q
+// for u < 0; phi(u) = e^{-x^2} / sqrt(2 pi) reuses the same exponential. In fp32
+// with the hardware ex2/rcp approximations the CDF error stays below 1e-6, far
+// under the bf16 output spacing.
+struct NormalCdfPdf {
+    float cdf, pdf;
+};
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ NormalCdfPdf normal_cdf_pdf(float u) {
+    const float x = fabsf(u) * 0.70710678118654752f;
+    const float s = rcp_approx(fmaf(0.3275911f, x, 1.0f));
+    float poly = fmaf(1.061405429f, s, -1.453152027f);
+    poly = fmaf(poly, s, 1.421413741f);
+    poly = fmaf(poly, s, -0.284496736f);
+    poly = fmaf(poly, s, 0.254829592f);
+    poly *= s;
+    const float e = ex2_approx(-(x * x) * 1.4426950408889634f);  // e^{-x^2}
+    const float q = 0.5f * poly * e;
+    return {u >= 0.0f ? 1.0f - q : q, 0.39894228040143268f * e};
 }
 
+// GeLU(u) = u Phi(u) (erf form).
+__device__ __forceinline__ float gelu_f(float u) { return u * normal_cdf_pdf(u).cdf; }
+
+// GeLU'(u) = Phi(u) + u phi(u).
 __device__ __forceinline__ float gelu_prime_f(float u) {
-    const float cdf = 0.5f * (1.0f + erff(u * 0.70710678118654752f));
-    const float pdf = 0.39894228040143268f * expf(-0.5f * u * u);
-    return cdf + u * pdf;
+    const NormalCdfPdf c = normal_cdf_pdf(u);
+    return fmaf(u, c.pdf, c.cdf);
 }
 
-__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&p)[16]) {
-    uint4* d = reinterpret_cast<uint4*>(dst);
-    d[0] = make_uint4(p[0], p[1], p[2], p[3]);
-    d[1] = make_uint4(p[4], p[5], p[6], p[7]);
-    d[2] = make_uint4(p[8], p[9], p[10], p[11]);
-    d[3] = make_uint4(p[12], p[13], p[14], p[15]);
+// One warp writes its 32 rows x 32 columns of bf16 (thread = row) into one of its
+// two staging boxes, in the 64-byte-swizzled layout the output tensor map uses
+// (16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3)), then lane 0 stores
+// the box with TMA at (x = first column, y = first row). Out-of-range rows and
+// columns are clipped by the TMA unit.
+__device__ __forceinline__ void stage_and_store(const CUtensorMap* map, uint8_t* stg, int& sbuf, int lane,
+                                                const uint32_t (&p)[16], int x, int y) {
+    if (lane == 0) bulk_wait_group_read<1>();  // the store that last used this box has read it
+    __syncwarp();
+    uint8_t* row = stg + sbuf * 2048 + lane * 64;
+    const int sw = (lane >> 1) & 3;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(row + ((j ^ sw) << 4)) = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(map, stg + sbuf * 2048, x, y);
+        bulk_commit_group();
+    }
+    sbuf ^= 1;
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__device__ __forceinline__ void decode_unit(const GemmArgs& a, int u, int& m_blk, int& ucol) {
+    if (a.n_fastest) {
+        const int ncols = a.num_units / a.num_m_blocks;
+        ucol = u % ncols;
+        m_blk = u / ncols;
+    } else {
+        m_blk = u % a.num_m_blocks;
+        ucol = u / a.num_m_blocks;
+    }
+}
+
+template <int BN, bool A_MN, bool B_MN, int EPI, int NE>
+__global__ void __launch_bounds__(GemmCfg<BN, EPI, NE>::NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                    const GemmArgs args) {
-    using Cfg = GemmCfg<BN>;
+    using Cfg = GemmCfg<BN, EPI, NE>;
     constexpr int STAGES = Cfg::STAGES;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::STAGE_BYTES);
+    uint8_t* stg_base = smem + STAGES * Cfg::STAGE_BYTES;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(stg_base + Cfg::STG_BYTES);
     uint64_t* full_bar = bars;
     uint64_t* empty_bar = bars + STAGES;
     uint64_t* tfull_bar = bars + 2 * STAGES;
@@ -174,7 +239,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull_bar[b], 1);
-            mbar_init(&tempty_bar[b], NUM_EPI_WARPS);
+            mbar_init(&tempty_bar[b], NE);
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0u;
@@ -184,6 +249,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB);
+        if (EPI != EPI_CE) {
+            prefetch_tensormap(&tmO0);
+            if (EPI == EPI_GELU) prefetch_tensormap(&tmO1);
+        }
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -203,8 +272,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x) {
-                const int m_blk = u % args.num_m_blocks;
-                const int n_blk0 = (u / args.num_m_blocks) * args.tiles_per_unit;
+                int m_blk, ucol;
+                decode_unit(args, u, m_blk, ucol);
+                const int n_blk0 = ucol * args.tiles_per_unit;
                 for (int nt = 0; nt < args.tiles_per_unit && ok; ++nt) {
                     const int n_blk = n_blk0 + nt;
                     for (int kb = args.kb_begin; kb < args.kb_end; ++kb) {
@@ -291,17 +361,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             wait_drain(drain_bar, 0, args.status);
         }
     } else {
-        // ---------------- epilogue (warps 2..5) ----------------
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        // ---------------- epilogue (NE warps) ----------------
+        constexpr int CHUNKS = BN / 32;
+        constexpr int MY_CHUNKS = CHUNKS / (NE / 4);
+        const int e = warp - 2;                      // epilogue warp index
+        const int q = warp & 3;                      // TMEM lane quarter this warp may access
+        const int c_begin = (e >> 2) * MY_CHUNKS;    // column half (8 warps) or all columns (4)
         const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+        uint8_t* stg = stg_base + e * STG_BYTES_PER_WARP;
+        int sbuf = 0;
         uint32_t tcount = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x) {
-            const int m_blk = u % args.num_m_blocks;
-            const int ucol = u / args.num_m_blocks;
+            int m_blk, ucol;
+            decode_unit(args, u, m_blk, ucol);
             const int n_blk0 = ucol * args.tiles_per_unit;
-            const int row = m_blk * BM + row_in_tile;
+            const int row0 = m_blk * BM + q * 32;    // first row of this warp's 32 rows
+            const int row = row0 + lane;
             const bool row_ok = row < args.M;
             // cross-entropy running state (natural-log units)
             float run_m = -INFINITY, run_s = 0.0f, z_tgt = 0.0f;
@@ -321,39 +398,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 tc_fence_after();
                 const int n_blk = n_blk0 + nt;
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int cc = 0; cc < MY_CHUNKS; ++cc) {
+                    const int c = c_begin + cc;
                     const int col0 = n_blk * BN + c * 32;
-                    uint32_t r[32];
-                    tmem_ld32(tmem_base + lane_addr + buf * BN + c * 32, r);
-                    tmem_ld_wait(r);
-                    if (col0 >= args.N) continue;  // ragged N tail (whole 32-column chunks)
-                    if constexpr (EPI == EPI_STORE) {
-                        if (row_ok) {
-                            uint32_t p[16];
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                p[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                            store_row32(args.out0 + row * args.ld0 + col0, p);
-                        }
-                    } else if constexpr (EPI == EPI_GELU) {
-                        if (row_ok) {
-                            uint32_t p[16];
-                            if (args.out1 != nullptr) {
-#pragma unroll
-                                for (int j = 0; j < 16; ++j)
-                                    p[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                                store_row32(args.out1 + row * args.ld1 + col0, p);
-                            }
-#pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                p[j] = pack_bf16x2(gelu_f(__uint_as_float(r[2 * j])),
-                                                   gelu_f(__uint_as_float(r[2 * j + 1])));
-                            store_row32(args.out0 + row * args.ld0 + col0, p);
-                        }
-                    } else if constexpr (EPI == EPI_DGELU) {
-                        if (row_ok) {
+                    uint32_t uw[16];
+                    if constexpr (EPI == EPI_DGELU) {
+                        // U row segment for GeLU'(U); issued before the TMEM load to overlap.
+                        if (row_ok && col0 < args.N) {
                             const uint4* src = reinterpret_cast<const uint4*>(args.aux + row * args.ld_aux + col0);
-                            uint32_t uw[16];
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const uint4 w = src[j];
@@ -362,15 +414,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 uw[4 * j + 2] = w.z;
                                 uw[4 * j + 3] = w.w;
                             }
-                            uint32_t p[16];
+                        } else {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const float g0 = __uint_as_float(r[2 * j]) * gelu_prime_f(bf16_lo(uw[j]));
-                                const float g1 = __uint_as_float(r[2 * j + 1]) * gelu_prime_f(bf16_hi(uw[j]));
-                                p[j] = pack_bf16x2(g0, g1);
-                            }
-                            store_row32(args.out0 + row * args.ld0 + col0, p);
+                            for (int j = 0; j < 16; ++j) uw[j] = 0u;
                         }
+                    }
+                    uint32_t r[32];
+                    tmem_ld32(tmem_base + lane_addr + buf * BN + c * 32, r);
+                    tmem_ld_wait(r);
+                    if (cc == MY_CHUNKS - 1) {
+                        // Last columns of this accumulator are in registers: hand it back to the MMA.
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+                    }
+                    if (col0 >= args.N) continue;  // ragged N tail (whole 32-column chunks)
+                    if constexpr (EPI == EPI_STORE) {
+                        uint32_t p[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            p[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                        stage_and_store(&tmO0, stg, sbuf, lane, p, col0, row0);
+                    } else if constexpr (EPI == EPI_GELU) {
+                        uint32_t p[16];
+                        if (args.out1 != nullptr) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                p[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                            stage_and_store(&tmO1, stg, sbuf, lane, p, col0, row0);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j)
+                            p[j] = pack_bf16x2(gelu_f(__uint_as_float(r[2 * j])), gelu_f(__uint_as_float(r[2 * j + 1])));
+                        stage_and_store(&tmO0, stg, sbuf, lane, p, col0, row0);
+                    } else if constexpr (EPI == EPI_DGELU) {
+                        uint32_t p[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const float g0 = __uint_as_float(r[2 * j]) * gelu_prime_f(bf16_lo(uw[j]));
+                            const float g1 = __uint_as_float(r[2 * j + 1]) * gelu_prime_f(bf16_hi(uw[j]));
+                            p[j] = pack_bf16x2(g0, g1);
+                        }
+                        stage_and_store(&tmO0, stg, sbuf, lane, p, col0, row0);
                     } else {  // EPI_CE
                         const int lim = args.v_valid - col0;  // valid columns in this chunk
                         if (lim > 0) {
@@ -389,8 +474,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             float acc = 0.0f;
 #pragma unroll
                             for (int j = 0; j < 32; ++j) {
-                                const float e = ex2_approx(fmaf(__uint_as_float(r[j]), LOG2E, -mb));
-                                acc += (j < lim) ? e : 0.0f;
+                                const float ev = ex2_approx(fmaf(__uint_as_float(r[j]), LOG2E, -mb));
+                                acc += (j < lim) ? ev : 0.0f;
                             }
                             run_s += acc;
                             const unsigned dt = static_cast<unsigned>(tgt - col0);
@@ -402,9 +487,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty_bar[buf]);
             }
             if (!ok) break;
             if constexpr (EPI == EPI_CE) {
@@ -416,6 +498,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
         }
+        // All of this warp's TMA stores must have landed before the kernel ends.
+        if (EPI != EPI_CE && lane == 0) bulk_wait_group<0>();
     }
 
     // ---------------- teardown ----------------
@@ -429,17 +513,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // Host-side launcher (grid = min(units, SMs), one CTA per SM).
-template <int BN, bool A_MN, bool B_MN, int EPI>
-inline cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& args,
-                                  int num_sms, cudaStream_t stream) {
-    using Cfg = GemmCfg<BN>;
-    auto kern = gemm_tc_kernel<BN, A_MN, B_MN, EPI>;
+template <int BN, bool A_MN, bool B_MN, int EPI, int NE>
+inline cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO0,
+                                  const CUtensorMap& tmO1, const GemmArgs& args, int num_sms, cudaStream_t stream) {
+    using Cfg = GemmCfg<BN, EPI, NE>;
+    auto kern = gemm_tc_kernel<BN, A_MN, B_MN, EPI, NE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_BYTES));
     if (e != cudaSuccess) return e;
     const int grid = args.num_units < num_sms ? args.num_units : num_sms;
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, args);
+    kern<<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmO0, tmO1, args);
     return cudaGetLastError();
 }
 

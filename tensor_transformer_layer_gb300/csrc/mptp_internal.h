@@ -7,7 +7,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/mptp.h"
+#include "mptp.h"
 
 namespace mptp {
 
@@ -16,6 +16,15 @@ namespace mptp {
 // zero fill out of bounds. Returns false if the driver rejects it.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
                     uint32_t box_inner, uint32_t box_outer);
+
+// Tensor map for an epilogue output: 32 x 32 boxes, 64-byte swizzle (the layout
+// the epilogue stages rows in before its TMA store).
+bool make_tmap_bf16_out(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems);
+
+// Unit order for a GEMM whose A operand (M side) has a_bytes and B operand (N side)
+// b_bytes: walk the smaller operand's blocks fastest, so it stays resident in L2
+// while concurrent CTAs share the slices of the larger one.
+inline int n_fastest_order(double a_bytes, double b_bytes) { return b_bytes < a_bytes ? 1 : 0; }
 
 // MP_OK if the current device is compute capability 10.3; fills the SM count.
 mp_status check_device(int* num_sms);
