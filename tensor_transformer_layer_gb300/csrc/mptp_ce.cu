@@ -69,12 +69,12 @@ extern "C" mp_status mp_vocab_ce_partials(const mp_bf16* X, const mp_bf16* E, co
     ce_plan(v_pad, t, &plan);
 
     CUtensorMap tmX, tmE;
-    if (!make_tmap_bf16(&tmX, X, h, T, h, 64, BM) || !make_tmap_bf16(&tmE, E, h, v_pad, h, 64, plan.bn))
+    if (!make_tmap_bf16(&tmX, X, h, T, h, 64, BM) || !make_tmap_bf16(&tmE, E, h, v_pad, h, 64, plan.bn / 2))
         return MP_ERR_CUDA;
     GemmArgs a{};
     a.M = T;
     a.N = v_pad;
-    a.num_m_blocks = ceil_div(T, BM);
+    a.num_m_blocks = ceil_div(T, 2 * BM);  // 256-row blocks: one per CTA-pair tile
     a.tiles_per_unit = plan.tiles_per_unit;
     a.num_units = a.num_m_blocks * plan.P;
     a.kb_begin = 0;

@@ -1,22 +1,31 @@
-// Persistent, warp-specialised tcgen05 GEMM for sm_103a with fused epilogues.
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a with fused epilogues,
+// run by CTA pairs (thread-block clusters of 2, tcgen05 cta_group::2).
 //
 //   C[M, N] = sum_k  A(m, k) * B(k, n),   bf16 inputs, fp32 accumulation in TMEM.
 //
-// One CTA per SM (grid = min(work units, SMs)); 64 + 32*NE threads:
-//   warp 0      TMA producer (one elected lane): 128x64 A tile + BNx64 B tile per
-//               stage into a STAGES-deep shared-memory ring, 128-byte swizzle.
-//   warp 1      TMEM allocator (whole warp) and MMA issuer (one lane): 4 x
-//               tcgen05.mma (M=128, N=BN, K=16) per stage into one of two TMEM
-//               accumulators (double buffer: 2*BN fp32 columns).
-//   warps 2..   NE epilogue warps (4 or 8): tcgen05.ld 32 rows x 32 columns per
-//               warp (TMEM lane quarter = warp % 4, thread = output row; with 8
-//               warps two warps share a quarter and split the columns), fused
-//               math, then bf16 rows staged in a 64-byte-swizzled shared buffer
-//               and written by TMA stores (32x32 boxes), or cross-entropy
-//               partials. Runs while the MMA fills the other accumulator; the
-//               accumulator is released as soon as its last columns are read.
+// A pair computes a 256 x BN output tile: CTA r (r = rank in the pair) owns rows
+// [256 i + 128 r, +128) of the tile and holds in its shared memory those 128 rows
+// of A and columns [BN/2 r, +BN/2) of B; the leader (r = 0) issues one
+// tcgen05.mma with M = 256 that reads both CTAs' shared memory and writes each
+// CTA's 128 x BN accumulator into that CTA's TMEM. Per SM this halves the B
+// traffic, so a stage is 32 KB (BN = 256) and the ring holds 6 stages.
 //
-// A work unit is one 128-row block and `tiles_per_unit` consecutive BN-wide
+// Grid = 2 x min(work units, co-resident pairs); 64 + 32*NE threads per CTA:
+//   warp 0      TMA producer (one lane) in each CTA: its A and B halves per
+//               stage, completion signalled on the leader's `full` barrier.
+//   warp 1      TMEM allocator (whole warp, both CTAs) and, in the leader only,
+//               the MMA issuer (one lane): 4 x tcgen05.mma (K = 16) per stage into
+//               one of two TMEM accumulators (2*BN fp32 columns per CTA); its
+//               commits arrive on the `empty` / `tmem full` barriers of both CTAs.
+//   warps 2..   NE epilogue warps (4 or 8) in each CTA: tcgen05.ld 32 rows x 32
+//               columns (TMEM lane quarter = warp % 4, thread = output row; with 8
+//               warps two warps share a quarter and split the columns), fused math,
+//               then bf16 rows staged in a 64-byte-swizzled shared box per warp and
+//               written by TMA stores (32x32 boxes), or cross-entropy partials. An
+//               accumulator is handed back (to the leader) as soon as its last
+//               columns are in registers, so it overlaps the next tile's MMAs.
+//
+// A work unit is one 256-row block and `tiles_per_unit` consecutive BN-wide
 // column tiles (1 for plain GEMMs; several for the cross-entropy, whose epilogue
 // keeps running per-row statistics over the unit). The K-loop runs over K
 // blocks [kb_begin, kb_end) in ascending order, so a K range that covers shards
@@ -28,8 +37,9 @@
 // with the 128-byte swizzle and described to the MMA without any transpose copy.
 //
 // Every mbarrier wait is bounded by a time budget; on expiry the kernel sets
-// MP_DEV_TIMEOUT in the status word, raises a CTA-wide abort flag, waits (with a
-// fixed bound) for its own TMA loads and MMAs in flight, frees TMEM and returns.
+// MP_DEV_TIMEOUT in the status word, raises a CTA-wide abort flag, lets its own
+// TMA loads and MMAs in flight finish (bounded), meets its peer at the cluster
+// barrier, frees TMEM and returns.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -38,13 +48,14 @@
 
 namespace mptp {
 
-constexpr int BM = 128;
-constexpr int BK = 64;
+constexpr int BM = 128;       // rows per CTA (a pair covers 2 * BM)
+constexpr int BK = 64;        // K per stage: one 128-byte swizzle row of bf16
 constexpr int UMMA_K = 16;
 constexpr int STG_BYTES_PER_WARP = 2 * 2048;  // two 32x32 bf16 staging boxes
 constexpr uint32_t DEV_TIMEOUT = 0x1u;
 constexpr uint32_t DEV_TARGET_RANGE = 0x2u;
 constexpr unsigned long long DRAIN_BUDGET_NS = 1000000000ull;  // 1 s
+constexpr unsigned long long ABORT_SETTLE_NS = 50000ull;       // in-flight copies land well within this
 
 enum EpiKind : int {
     EPI_STORE = 0,  // out0 = bf16(acc)
@@ -55,7 +66,7 @@ enum EpiKind : int {
 
 struct GemmArgs {
     int M, N;                 // output extent (masking of the ragged tails)
-    int num_m_blocks;         // ceil(M / BM)
+    int num_m_blocks;         // ceil(M / (2 * BM)): 256-row blocks, one per pair tile
     int num_units;            // num_m_blocks * unit columns
     int n_fastest;            // unit order: 0 = row blocks fastest, 1 = column units fastest
     int tiles_per_unit;       // BN-wide column tiles per unit
@@ -74,20 +85,27 @@ struct GemmArgs {
     unsigned long long budget_ns;
 };
 
+constexpr size_t SMEM_LIMIT = 232448;  // opt-in shared memory per block on sm_103
+
 template <int BN_, int EPI, int NE_>
 struct GemmCfg {
-    static constexpr int BN = BN_;
+    static constexpr int BN = BN_;             // tile width of the pair
+    static constexpr int BNH = BN / 2;         // B columns held per CTA
     static constexpr int NE = NE_;
     static constexpr int NUM_THREADS = 64 + 32 * NE;
     static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_BYTES = BNH * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
     static constexpr uint32_t TMEM_COLS = 2 * BN;
     static constexpr int STG_BYTES = (EPI == EPI_CE) ? 0 : NE * STG_BYTES_PER_WARP;
+    static constexpr int MAX_STAGES = 8;
+    static constexpr int FIT_STAGES = static_cast<int>((SMEM_LIMIT - 1024 - 512 - STG_BYTES) / STAGE_BYTES);
+    static constexpr int STAGES = FIT_STAGES < MAX_STAGES ? FIT_STAGES : MAX_STAGES;
     static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem full x2, tmem empty x2, drain
     static constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + STG_BYTES + 8 * NUM_BARS + 16;
-    static_assert(SMEM_BYTES <= 232448, "shared memory per block");
+    static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory per block");
+    static_assert(STAGES >= 4, "pipeline depth");
+    static_assert(BN == 128 || BN == 256, "pair tile width");
     static_assert(NE == 4 || NE == 8, "4 or 8 epilogue warps");
     static_assert(EPI != EPI_CE || NE == 4, "cross-entropy epilogue keeps one thread per row");
 };
@@ -98,14 +116,15 @@ struct Ctl {
     unsigned long long budget_ns;
 };
 
-// Bounded wait. false = gave up (budget spent or another role aborted).
+// Bounded wait. false = gave up (budget spent or another role of this CTA aborted).
 __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, const Ctl& c) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto probe = [&]() { return mbar_try_wait(bar, parity); };
+    if (probe()) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+            if (probe()) return true;
         if (*c.abort_flag) return false;
         if (globaltimer_ns() - t0 > c.budget_ns) {
             if (c.status) atomicOr(c.status, DEV_TIMEOUT);
@@ -124,6 +143,12 @@ __device__ __forceinline__ void wait_drain(uint64_t* bar, uint32_t parity, uint3
             if (status) atomicOr(status, DEV_TIMEOUT);
             return;
         }
+    }
+}
+
+__device__ __forceinline__ void spin_ns(unsigned long long ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < ns) {
     }
 }
 
@@ -208,12 +233,13 @@ __device__ __forceinline__ void decode_unit(const GemmArgs& a, int u, int& m_blk
 }
 
 template <int BN, bool A_MN, bool B_MN, int EPI, int NE>
-__global__ void __launch_bounds__(GemmCfg<BN, EPI, NE>::NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>::NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
                    const GemmArgs args) {
     using Cfg = GemmCfg<BN, EPI, NE>;
     constexpr int STAGES = Cfg::STAGES;
+    constexpr int BNH = Cfg::BNH;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -221,25 +247,29 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, NE>::NUM_THREADS, 1)
     uint8_t* sB = smem + STAGES * Cfg::A_BYTES;
     uint8_t* stg_base = smem + STAGES * Cfg::STAGE_BYTES;
     uint64_t* bars = reinterpret_cast<uint64_t*>(stg_base + Cfg::STG_BYTES);
-    uint64_t* full_bar = bars;
-    uint64_t* empty_bar = bars + STAGES;
-    uint64_t* tfull_bar = bars + 2 * STAGES;
-    uint64_t* tempty_bar = bars + 2 * STAGES + 2;
+    uint64_t* full_bar = bars;                // leader: both CTAs' loads of a stage landed
+    uint64_t* empty_bar = bars + STAGES;      // each CTA: the pair's MMAs finished reading a stage
+    uint64_t* tfull_bar = bars + 2 * STAGES;  // each CTA: accumulator ready
+    uint64_t* tempty_bar = bars + 2 * STAGES + 2;  // leader: both CTAs' epilogues drained an accumulator
     uint64_t* drain_bar = bars + 2 * STAGES + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = (rank == 0);
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&full_bar[s], 1);
+            mbar_init(&full_bar[s], 2);   // one expect_tx arrival from each CTA's producer
             mbar_init(&empty_bar[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull_bar[b], 1);
-            mbar_init(&tempty_bar[b], NE);
+            mbar_init(&tempty_bar[b], 2 * NE);  // every epilogue warp of both CTAs
         }
         mbar_init(drain_bar, 1);
         *abort_flag = 0u;
@@ -255,52 +285,52 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, NE>::NUM_THREADS, 1)
         }
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
+        tmem_relinquish_pair();
     }
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before any cross-CTA arrival
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const Ctl ctl{args.status, abort_flag, args.budget_ns};
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---------------- TMA producer ----------------
+            // ---------------- TMA producer (both CTAs) ----------------
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued_mask = 0, issued_parity = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x) {
+            for (int u = pair; u < args.num_units && ok; u += num_pairs) {
                 int m_blk, ucol;
                 decode_unit(args, u, m_blk, ucol);
                 const int n_blk0 = ucol * args.tiles_per_unit;
+                const int arow = m_blk * 2 * BM + static_cast<int>(rank) * BM;  // this CTA's A rows
                 for (int nt = 0; nt < args.tiles_per_unit && ok; ++nt) {
-                    const int n_blk = n_blk0 + nt;
+                    const int bcol = (n_blk0 + nt) * BN + static_cast<int>(rank) * BNH;  // this CTA's B columns
                     for (int kb = args.kb_begin; kb < args.kb_end; ++kb) {
                         if (!wait_bounded(&empty_bar[stage], phase ^ 1u, ctl)) {
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&full_bar[stage], Cfg::STAGE_BYTES);
+                        const uint32_t full_leader = mapa_shared(smem_u32(&full_bar[stage]), 0);
+                        mbar_arrive_expect_tx_cluster(full_leader, Cfg::STAGE_BYTES);
                         uint8_t* a_dst = sA + stage * Cfg::A_BYTES;
                         uint8_t* b_dst = sB + stage * Cfg::B_BYTES;
                         if (A_MN) {
 #pragma unroll
                             for (int j = 0; j < BM / 64; ++j)
-                                tma_load_2d(a_dst + j * 8192, &tmA, &full_bar[stage], m_blk * BM + j * 64, kb * BK);
+                                tma_load_2d_pair(a_dst + j * 8192, &tmA, full_leader, arow + j * 64, kb * BK);
                         } else {
-                            tma_load_2d(a_dst, &tmA, &full_bar[stage], kb * BK, m_blk * BM);
+                            tma_load_2d_pair(a_dst, &tmA, full_leader, kb * BK, arow);
                         }
                         if (B_MN) {
 #pragma unroll
-                            for (int j = 0; j < BN / 64; ++j)
-                                tma_load_2d(b_dst + j * 8192, &tmB, &full_bar[stage], n_blk * BN + j * 64, kb * BK);
+                            for (int j = 0; j < BNH / 64; ++j)
+                                tma_load_2d_pair(b_dst + j * 8192, &tmB, full_leader, bcol + j * 64, kb * BK);
                         } else {
-                            tma_load_2d(b_dst, &tmB, &full_bar[stage], kb * BK, n_blk * BN);
+                            tma_load_2d_pair(b_dst, &tmB, full_leader, kb * BK, bcol);
                         }
-                        issued_mask |= 1u << stage;
-                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
@@ -308,19 +338,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, NE>::NUM_THREADS, 1)
                     }
                 }
             }
-            // No TMA load of ours may still be landing when the CTA exits.
-            for (int s = 0; s < STAGES; ++s)
-                if (issued_mask & (1u << s)) wait_drain(&full_bar[s], (issued_parity >> s) & 1u, args.status);
+            // On an abort, give copies already issued time to land before the CTA can exit.
+            if (!ok) spin_ns(ABORT_SETTLE_NS);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---------------- MMA issuer ----------------
-            constexpr uint32_t IDESC = make_idesc_bf16(BM, BN, A_MN, B_MN);
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (leader CTA) ----------------
+            constexpr uint32_t IDESC = make_idesc_bf16(2 * BM, BN, A_MN, B_MN);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t tcount = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x) {
+            for (int u = pair; u < args.num_units && ok; u += num_pairs) {
                 for (int nt = 0; nt < args.tiles_per_unit && ok; ++nt, ++tcount) {
                     const uint32_t buf = tcount & 1u;
                     const uint32_t tph = (tcount >> 1) & 1u;
@@ -344,40 +373,39 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, NE>::NUM_THREADS, 1)
                                                      : make_sdesc_sw128(a_base + k * 32, 16, 1024);
                             const uint64_t bd = B_MN ? make_sdesc_sw128(b_base + k * 2048, 8192, 1024)
                                                      : make_sdesc_sw128(b_base + k * 32, 16, 1024);
-                            umma_bf16(d_tmem, ad, bd, IDESC, (kb > args.kb_begin || k > 0) ? 1u : 0u);
+                            umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > args.kb_begin || k > 0) ? 1u : 0u);
                         }
-                        umma_commit(&empty_bar[stage]);  // frees the stage when these MMAs finish
+                        umma_commit_pair_multicast(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    umma_commit(&tfull_bar[buf]);  // accumulator ready for the epilogue
+                    umma_commit_pair_multicast(&tfull_bar[buf], 0x3);  // accumulators ready in both CTAs
                 }
             }
-            // Every MMA of ours must finish before TMEM is freed.
-            umma_commit(drain_bar);
+            // Every MMA of the pair must finish before either CTA frees TMEM or exits.
+            umma_commit_pair(drain_bar);
             wait_drain(drain_bar, 0, args.status);
         }
     } else {
-        // ---------------- epilogue (NE warps) ----------------
+        // ---------------- epilogue (NE warps, both CTAs) ----------------
         constexpr int CHUNKS = BN / 32;
         constexpr int MY_CHUNKS = CHUNKS / (NE / 4);
         const int e = warp - 2;                      // epilogue warp index
         const int q = warp & 3;                      // TMEM lane quarter this warp may access
         const int c_begin = (e >> 2) * MY_CHUNKS;    // column half (8 warps) or all columns (4)
-        const int row_in_tile = q * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         uint8_t* stg = stg_base + e * STG_BYTES_PER_WARP;
         int sbuf = 0;
         uint32_t tcount = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < args.num_units && ok; u += gridDim.x) {
+        for (int u = pair; u < args.num_units && ok; u += num_pairs) {
             int m_blk, ucol;
             decode_unit(args, u, m_blk, ucol);
             const int n_blk0 = ucol * args.tiles_per_unit;
-            const int row0 = m_blk * BM + q * 32;    // first row of this warp's 32 rows
+            const int row0 = m_blk * 2 * BM + static_cast<int>(rank) * BM + q * 32;  // this warp's 32 rows
             const int row = row0 + lane;
             const bool row_ok = row < args.M;
             // cross-entropy running state (natural-log units)
@@ -423,10 +451,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, NE>::NUM_THREADS, 1)
                     tmem_ld32(tmem_base + lane_addr + buf * BN + c * 32, r);
                     tmem_ld_wait(r);
                     if (cc == MY_CHUNKS - 1) {
-                        // Last columns of this accumulator are in registers: hand it back to the MMA.
+                        // Last columns of this accumulator are in registers: hand it back to the leader's MMA.
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&tempty_bar[buf]);
+                        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[buf]), 0));
                     }
                     if (col0 >= args.N) continue;  // ragged N tail (whole 32-column chunks)
                     if constexpr (EPI == EPI_STORE) {
@@ -505,14 +533,38 @@ __global__ void __launch_bounds__(GemmCfg<BN, EPI, NE>::NUM_THREADS, 1)
     // ---------------- teardown ----------------
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // the leader's MMAs (which read this CTA's shared memory) are done
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+        tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
     }
 }
 
-// Host-side launcher (grid = min(units, SMs), one CTA per SM).
+// Number of CTA pairs that can be resident at once for one kernel instantiation.
+template <int BN, bool A_MN, bool B_MN, int EPI, int NE>
+inline int resident_pairs(int num_sms) {
+    using Cfg = GemmCfg<BN, EPI, NE>;
+    static int cached[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+    cfg.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<BN, A_MN, B_MN, EPI, NE>, &cfg) != cudaSuccess ||
+        clusters <= 0) {
+        cudaGetLastError();
+        clusters = num_sms / 2;
+    }
+    if (clusters > num_sms / 2) clusters = num_sms / 2;
+    if (dev >= 0 && dev < 64) cached[dev] = clusters;
+    return clusters;
+}
+
+// Host-side launcher: grid = 2 x min(units, resident pairs), one CTA per SM.
 template <int BN, bool A_MN, bool B_MN, int EPI, int NE>
 inline cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO0,
                                   const CUtensorMap& tmO1, const GemmArgs& args, int num_sms, cudaStream_t stream) {
@@ -521,9 +573,10 @@ inline cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    const int grid = args.num_units < num_sms ? args.num_units : num_sms;
-    if (grid <= 0) return cudaSuccess;
-    kern<<<grid, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmO0, tmO1, args);
+    const int pairs = resident_pairs<BN, A_MN, B_MN, EPI, NE>(num_sms);
+    const int use = args.num_units < pairs ? args.num_units : pairs;
+    if (use <= 0) return cudaSuccess;
+    kern<<<2 * use, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmO0, tmO1, args);
     return cudaGetLastError();
 }
 

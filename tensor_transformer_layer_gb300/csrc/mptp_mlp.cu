@@ -27,7 +27,7 @@ static GemmArgs base_args(int M, int N, int bn, int kb_begin, int kb_end, double
     GemmArgs a{};
     a.M = M;
     a.N = N;
-    a.num_m_blocks = ceil_div(M, BM);
+    a.num_m_blocks = ceil_div(M, 2 * BM);  // 256-row blocks: one per CTA-pair tile
     a.tiles_per_unit = 1;
     a.num_units = a.num_m_blocks * ceil_div(N, bn);
     a.n_fastest = n_fastest_order(a_bytes, b_bytes);
@@ -108,7 +108,7 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
     // K3: dU = (dZ B^T) * GeLU'(U).  A operand dZ [T,h] (K-major), B operand B [f,h] (K-major).
     const double Tb = 2.0 * T, hb = 2.0 * h, fb = 2.0 * f;
     CUtensorMap tm_dZ_k, tm_B_k, tm_dU_o;
-    if (!make_tmap_bf16(&tm_dZ_k, dZ, h, T, h, 64, BM) || !make_tmap_bf16(&tm_B_k, B, h, f, h, 64, 256) ||
+    if (!make_tmap_bf16(&tm_dZ_k, dZ, h, T, h, 64, BM) || !make_tmap_bf16(&tm_B_k, B, h, f, h, 64, 128) ||
         !make_tmap_bf16_out(&tm_dU_o, dU_ws, f, T, f))
         return MP_ERR_CUDA;
     GemmArgs a3 = base_args(T, f, 256, 0, h / BK, Tb * h, fb * h, d_status);
@@ -122,7 +122,7 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
 
     // K4: dX = sum_i dU_i A_i^T.  A operand dU [T,f] (K-major), B operand A [h,f] (K-major).
     CUtensorMap tm_dU_k, tm_A_k, tm_dX_o;
-    if (!make_tmap_bf16(&tm_dU_k, dU_ws, f, T, f, 64, BM) || !make_tmap_bf16(&tm_A_k, A, f, h, f, 64, 256) ||
+    if (!make_tmap_bf16(&tm_dU_k, dU_ws, f, T, f, 64, BM) || !make_tmap_bf16(&tm_A_k, A, f, h, f, 64, 128) ||
         !make_tmap_bf16_out(&tm_dX_o, dX, h, T, h))
         return MP_ERR_CUDA;
     const int fs = f / t;
