@@ -190,18 +190,21 @@ def summarize_clocks(text: str):
 class Step:
     """Device buffers and the C-ABI calls of one step."""
 
-    def __init__(self, dev):
+    def __init__(self, dev, host_in=None):
         import torch
 
         import synth
         import tensor_transformer_layer_gb300 as mp
         self.mp = mp
         self.torch = torch
+        self.dev = dev
         m, c = MLP, CE
-        mi = synth.mlp_inputs(m["T"], m["h"], m["f"], m["seed"])
-        ci = synth.ce_inputs(c["T"], c["h"], c["v_pad"], c["v_valid"], c["seed"])
-        self.host_in = {"X": mi["X"], "A": mi["A"], "B": mi["B"], "dZ": mi["dZ"], "Xc": ci["X"], "E": ci["E"],
-                        "target": ci["target"]}
+        if host_in is None:
+            mi = synth.mlp_inputs(m["T"], m["h"], m["f"], m["seed"])
+            ci = synth.ce_inputs(c["T"], c["h"], c["v_pad"], c["v_valid"], c["seed"])
+            host_in = {"X": mi["X"], "A": mi["A"], "B": mi["B"], "dZ": mi["dZ"], "Xc": ci["X"], "E": ci["E"],
+                       "target": ci["target"]}
+        self.host_in = host_in
         self.d = {k: v.to(dev) for k, v in self.host_in.items()}
         T, h, f = m["T"], m["h"], m["f"]
         bf = torch.bfloat16
@@ -212,21 +215,25 @@ class Step:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out_names = ("Z", "dX", "dA", "dB", "loss")
 
-    def run(self, ev=None):
-        """One step. ev: optional dict of CUDA events to record around the CE logit kernel."""
+    def twin(self):
+        """Same host inputs, its own device buffers (for double-buffered pipelines)."""
+        return Step(self.dev, host_in=self.host_in)
+
+    def run(self, ev=None, stream=None):
+        """One step on `stream` (default: the current stream). ev: optional dict of CUDA
+        events to record around the CE logit kernel."""
         mp, d = self.mp, self.d
         t = MLP["t"]
-        mp.mp_mlp_fwd(d["X"], d["A"], d["B"], d["Z"], d["Y"], d["U"], t=t, d_status=self.status)
-        mp.mp_mlp_bwd(d["X"], d["A"], d["B"], d["U"], d["Y"], d["dZ"], d["dX"], d["dA"], d["dB"], d["dU"], t=t,
-                      d_status=self.status)
+        kw = dict(d_status=self.status, stream=stream)
+        mp.mp_mlp_fwd(d["X"], d["A"], d["B"], d["Z"], d["Y"], d["U"], t=t, **kw)
+        mp.mp_mlp_bwd(d["X"], d["A"], d["B"], d["U"], d["Y"], d["dZ"], d["dX"], d["dA"], d["dB"], d["dU"], t=t, **kw)
         if ev is not None:
             ev["ce0"].record()
-        mp.mp_vocab_ce_partials(d["Xc"], d["E"], d["target"], self.ws, v_valid=CE["v_valid"], t=CE["t"],
-                                d_status=self.status)
+        mp.mp_vocab_ce_partials(d["Xc"], d["E"], d["target"], self.ws, v_valid=CE["v_valid"], t=CE["t"], **kw)
         if ev is not None:
             ev["ce1"].record()
         mp.mp_vocab_ce_combine(self.ws, d["target"], d["loss"], v_pad=CE["v_pad"], v_valid=CE["v_valid"],
-                               t=CE["t"], d_status=self.status)
+                               t=CE["t"], **kw)
 
     def check_status(self):
         s = int(self.status.item())
@@ -284,29 +291,55 @@ def time_breakdown(step, reps, flush):
 
 
 def time_e2e(step, steps, warmup):
-    """Same step through the same calls, with pinned host inputs copied in and results copied out."""
+    """The step through the same C-ABI calls with every input copied in from pinned host
+    memory and every result (Z, dX, dA, dB, loss) copied back, all inside the timed
+    region. Copies and compute run as a double-buffered pipeline on three streams:
+    step i+1's inputs go in and step i-1's results come out while step i computes."""
     import torch
     host_in = {k: v.pin_memory() for k, v in step.host_in.items()}
     host_out = {k: torch.empty(step.d[k].shape, dtype=step.d[k].dtype).pin_memory() for k in step.out_names}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    sets = [step, step.twin()]
+    s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    cur = torch.cuda.current_stream()
+    for e in ev_comp + ev_out:
+        e.record(cur)
 
-    def one():
-        for k, v in host_in.items():
-            step.d[k].copy_(v, non_blocking=True)
-        step.run()
-        for k, v in host_out.items():
-            v.copy_(step.d[k], non_blocking=True)
+    def one(i):
+        b = i % 2
+        st = sets[b]
+        s_in.wait_event(ev_comp[b])          # buffer set b's previous step no longer reads its inputs
+        with torch.cuda.stream(s_in):
+            for k, v in host_in.items():
+                st.d[k].copy_(v, non_blocking=True)
+        ev_in[b].record(s_in)
+        s_comp.wait_event(ev_in[b])
+        s_comp.wait_event(ev_out[b])         # its previous results have been copied out
+        st.run(stream=s_comp)
+        ev_comp[b].record(s_comp)
+        s_out.wait_event(ev_comp[b])
+        with torch.cuda.stream(s_out):
+            for k, v in host_out.items():
+                v.copy_(st.d[k], non_blocking=True)
+        ev_out[b].record(s_out)
 
-    for _ in range(warmup):
-        one()
+    for i in range(warmup):
+        one(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(steps):
-        one()
-    b.record()
+    a.record(s_in)
+    for i in range(steps):
+        one(i)
+    s_in.wait_event(ev_out[0])
+    s_in.wait_event(ev_out[1])
+    b.record(s_in)
     torch.cuda.synchronize()
+    for st in sets:
+        st.check_status()
     return a.elapsed_time(b) / steps, h2d, d2h
 
 
@@ -461,10 +494,11 @@ def main(argv=None):
 
     e2e = None
     if not args.no_e2e:
-        e2e_ms, h2d, d2h = time_e2e(step, max(3, min(args.steps, 20)), 2)
+        e2e_ms, h2d, d2h = time_e2e(step, max(3, min(args.steps, 30)), 3)
         e2e_ms = max_over_ranks(e2e_ms, world, dev)
         e2e = {"value": world * step_flop() / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "pipeline": "double-buffered: H2D of step i+1 and D2H of step i-1 overlap step i's compute"}
     step.check_status()
 
     cpu = None

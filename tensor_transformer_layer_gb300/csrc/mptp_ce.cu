@@ -13,18 +13,34 @@
 
 namespace mptp {
 
-__global__ void ce_combine_kernel(const float* __restrict__ ws, const int32_t* __restrict__ target,
-                                  float* __restrict__ loss, int T, int P, int chunk_cols, int v_valid,
-                                  uint32_t* status) {
+__global__ void __launch_bounds__(128) ce_combine_kernel(const float* __restrict__ ws, const int32_t* __restrict__ target,
+                                                         float* __restrict__ loss, int T, int P, int chunk_cols,
+                                                         int v_valid, uint32_t* status) {
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= T) return;
     const long long stride = 3ll * T;
-    float M = -INFINITY;
-    for (int p = 0; p < P; ++p) M = fmaxf(M, ws[p * stride + r]);
-    float S = 0.0f;
-    for (int p = 0; p < P; ++p) {
-        const float sp = ws[p * stride + T + r];
-        if (sp > 0.0f) S += sp * expf(ws[p * stride + r] - M);
+    // One pass over the partitions, 8 at a time (independent loads in flight):
+    // M = max_p m_p, S = sum_p s_p exp(m_p - M) with the running sum rescaled when M
+    // grows; partitions holding no valid column (s_p = 0, m_p = -inf) are skipped.
+    float M = -INFINITY, S = 0.0f;
+    for (int p0 = 0; p0 < P; p0 += 8) {
+        float mm[8], ss[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int p = p0 + j;
+            mm[j] = (p < P) ? ws[p * stride + r] : -INFINITY;
+            ss[j] = (p < P) ? ws[p * stride + T + r] : 0.0f;
+        }
+        float cm = mm[0];
+#pragma unroll
+        for (int j = 1; j < 8; ++j) cm = fmaxf(cm, mm[j]);
+        const float nM = fmaxf(M, cm);
+        if (nM == -INFINITY) continue;
+        S = (M == -INFINITY) ? 0.0f : S * expf(M - nM);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (ss[j] > 0.0f) S += ss[j] * expf(mm[j] - nM);
+        M = nM;
     }
     const int tg = target[r];
     if (tg < 0 || tg >= v_valid) {
@@ -106,7 +122,7 @@ extern "C" mp_status mp_vocab_ce_combine(const void* workspace, size_t workspace
     if (st != MP_OK) return st;
     CePlan plan;
     ce_plan(v_pad, t, &plan);
-    const int threads = 256;
+    const int threads = 128;
     ce_combine_kernel<<<ceil_div(T, threads), threads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const float*>(workspace), target, loss, T, plan.P, plan.chunk_cols, v_valid, d_status);
     return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;

@@ -425,38 +425,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                 }
                 tc_fence_after();
                 const int n_blk = n_blk0 + nt;
-#pragma unroll 1
-                for (int cc = 0; cc < MY_CHUNKS; ++cc) {
+                // Chunk pipeline: the TMEM load (and, for GeLU', the U row segment) of
+                // chunk cc+1 is in flight while chunk cc is computed and stored.
+                auto issue = [&](int cc, uint32_t (&rr)[32], uint32_t (&uu)[16]) {
                     const int c = c_begin + cc;
-                    const int col0 = n_blk * BN + c * 32;
-                    uint32_t uw[16];
                     if constexpr (EPI == EPI_DGELU) {
-                        // U row segment for GeLU'(U); issued before the TMEM load to overlap.
+                        const int col0 = n_blk * BN + c * 32;
                         if (row_ok && col0 < args.N) {
                             const uint4* src = reinterpret_cast<const uint4*>(args.aux + row * args.ld_aux + col0);
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
                                 const uint4 w = src[j];
-                                uw[4 * j + 0] = w.x;
-                                uw[4 * j + 1] = w.y;
-                                uw[4 * j + 2] = w.z;
-                                uw[4 * j + 3] = w.w;
+                                uu[4 * j + 0] = w.x;
+                                uu[4 * j + 1] = w.y;
+                                uu[4 * j + 2] = w.z;
+                                uu[4 * j + 3] = w.w;
                             }
                         } else {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) uw[j] = 0u;
+                            for (int j = 0; j < 16; ++j) uu[j] = 0u;
                         }
                     }
-                    uint32_t r[32];
-                    tmem_ld32(tmem_base + lane_addr + buf * BN + c * 32, r);
-                    tmem_ld_wait(r);
-                    if (cc == MY_CHUNKS - 1) {
-                        // Last columns of this accumulator are in registers: hand it back to the leader's MMA.
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[buf]), 0));
-                    }
-                    if (col0 >= args.N) continue;  // ragged N tail (whole 32-column chunks)
+                    tmem_ld32(tmem_base + lane_addr + buf * BN + c * 32, rr);
+                };
+                auto finish = [&](int cc, const uint32_t (&r)[32], const uint32_t (&uw)[16]) {
+                    const int c = c_begin + cc;
+                    const int col0 = n_blk * BN + c * 32;
+                    if (col0 >= args.N) return;  // ragged N tail (whole 32-column chunks)
                     if constexpr (EPI == EPI_STORE) {
                         uint32_t p[16];
 #pragma unroll
@@ -514,6 +509,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                             }
                         }
                     }
+                };
+                // Last columns of this accumulator are in registers: hand it back to the leader's MMA.
+                auto release = [&]() {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[buf]), 0));
+                };
+                uint32_t ra[32], rb[32], ua[16], ub[16];
+                issue(0, ra, ua);
+#pragma unroll 1
+                for (int cc = 0; cc < MY_CHUNKS; cc += 2) {
+                    tmem_ld_wait(ra);
+                    issue(cc + 1, rb, ub);
+                    finish(cc, ra, ua);
+                    tmem_ld_wait(rb);
+                    if (cc + 2 < MY_CHUNKS)
+                        issue(cc + 2, ra, ua);
+                    else
+                        release();
+                    finish(cc + 1, rb, ub);
                 }
             }
             if (!ok) break;
