@@ -338,8 +338,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                     }
                 }
             }
-            // On an abort, give copies already issued time to land before the CTA can exit.
-            if (!ok) spin_ns(ABORT_SETTLE_NS);
         }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
@@ -548,6 +546,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
     // ---------------- teardown ----------------
     tc_fence_before();
     __syncthreads();
+    // After an abort some TMA loads issued by this CTA may never have been consumed;
+    // give them a fixed time to land before this CTA (or, via the cluster barrier,
+    // the leader whose barrier they signal) can exit. The flag is final here.
+    if (*abort_flag) {
+        if (threadIdx.x == 0) spin_ns(ABORT_SETTLE_NS);
+        __syncthreads();
+    }
     cluster_sync_all();  // the leader's MMAs (which read this CTA's shared memory) are done
     if (warp == 1) {
         __syncwarp();
