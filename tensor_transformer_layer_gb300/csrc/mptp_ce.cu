@@ -84,25 +84,28 @@ extern "C" mp_status mp_vocab_ce_partials(const mp_bf16* X, const mp_bf16* E, co
     CePlan plan;
     ce_plan(v_pad, t, &plan);
 
-    CUtensorMap tmX, tmE;
-    if (!make_tmap_bf16(&tmX, X, h, T, h, 64, BM) || !make_tmap_bf16(&tmE, E, h, v_pad, h, 64, plan.bn / 2))
+    TmapSet m{};
+    if (!make_tmap_bf16(&m.a, X, h, T, h, 64, BM) || !make_tmap_bf16(&m.b, E, h, v_pad, h, 64, plan.bn / 2))
         return MP_ERR_CUDA;
     GemmArgs a{};
-    a.M = T;
-    a.N = v_pad;
-    a.num_m_blocks = ceil_div(T, 2 * BM);  // 256-row blocks: one per CTA-pair tile
+    a.pr.M = T;
+    a.pr.N = v_pad;
+    a.pr.num_m_blocks = ceil_div(T, 2 * BM);  // 256-row blocks: one per CTA-pair tile
+    a.pr.num_units = a.pr.num_m_blocks * plan.P;
+    a.pr.n_fastest = 0;
+    a.pr.kb_begin = 0;
+    a.pr.kb_end = h / BK;
+    a.pr.a_mn = 0;
+    a.pr.b_mn = 0;
     a.tiles_per_unit = plan.tiles_per_unit;
-    a.num_units = a.num_m_blocks * plan.P;
-    a.kb_begin = 0;
-    a.kb_end = h / BK;
     a.target = target;
     a.ws = static_cast<float*>(workspace);
     a.v_valid = v_valid;
     a.status = d_status;
     a.budget_ns = wait_budget_ns();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = (plan.bn == 256) ? launch_gemm_tc<256, false, false, EPI_CE, 4>(tmX, tmE, tmX, tmX, a, sms, s)
-                                     : launch_gemm_tc<128, false, false, EPI_CE, 4>(tmX, tmE, tmX, tmX, a, sms, s);
+    cudaError_t e = (plan.bn == 256) ? launch_gemm_tc<256, EPI_CE, 4>(m, a, sms, s)
+                                     : launch_gemm_tc<128, EPI_CE, 4>(m, a, sms, s);
     return e == cudaSuccess ? MP_OK : MP_ERR_CUDA;
 }
 

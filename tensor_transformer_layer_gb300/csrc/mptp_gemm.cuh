@@ -64,25 +64,37 @@ enum EpiKind : int {
     EPI_CE = 3,     // per-row online max / sum-exp / target logit over the unit
 };
 
-struct GemmArgs {
+// The GEMM of a launch.
+struct ProbInfo {
     int M, N;                 // output extent (masking of the ragged tails)
     int num_m_blocks;         // ceil(M / (2 * BM)): 256-row blocks, one per pair tile
     int num_units;            // num_m_blocks * unit columns
     int n_fastest;            // unit order: 0 = row blocks fastest, 1 = column units fastest
-    int tiles_per_unit;       // BN-wide column tiles per unit
     int kb_begin, kb_end;     // K blocks (of BK) to accumulate, ascending
-    __nv_bfloat16* out0;
-    long long ld0;
-    __nv_bfloat16* out1;
-    long long ld1;
-    const __nv_bfloat16* aux;
+    int a_mn, b_mn;           // operand majorness: 1 = M (N) contiguous, 0 = K contiguous
+};
+
+struct GemmArgs {
+    ProbInfo pr;
+    int tiles_per_unit;       // BN-wide column tiles per unit (cross-entropy: several)
+    // epilogue operands that are not written through tensor maps
+    const __nv_bfloat16* aux; // U for GeLU'
     long long ld_aux;
+    int has_out1;             // GeLU: also store U (tensor map o1)
     // cross-entropy epilogue
     const int32_t* target;
     float* ws;                // [P][3][M] fp32: max, sum-exp, target logit
     int v_valid;
     uint32_t* status;         // nullable
     unsigned long long budget_ns;
+};
+
+// Tensor maps of a launch: the two operands and the epilogue outputs.
+struct alignas(64) TmapSet {
+    CUtensorMap a;
+    CUtensorMap b;
+    CUtensorMap o0;
+    CUtensorMap o1;
 };
 
 constexpr size_t SMEM_LIMIT = 232448;  // opt-in shared memory per block on sm_103
@@ -221,22 +233,20 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap* map, uint8_t*
     sbuf ^= 1;
 }
 
-__device__ __forceinline__ void decode_unit(const GemmArgs& a, int u, int& m_blk, int& ucol) {
-    if (a.n_fastest) {
-        const int ncols = a.num_units / a.num_m_blocks;
-        ucol = u % ncols;
-        m_blk = u / ncols;
+__device__ __forceinline__ void decode_unit(const ProbInfo& p, int lu, int& m_blk, int& ucol) {
+    if (p.n_fastest) {
+        const int ncols = p.num_units / p.num_m_blocks;
+        ucol = lu % ncols;
+        m_blk = lu / ncols;
     } else {
-        m_blk = u % a.num_m_blocks;
-        ucol = u / a.num_m_blocks;
+        m_blk = lu % p.num_m_blocks;
+        ucol = lu / p.num_m_blocks;
     }
 }
 
-template <int BN, bool A_MN, bool B_MN, int EPI, int NE>
+template <int BN, int EPI, int NE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>::NUM_THREADS, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmO0, const __grid_constant__ CUtensorMap tmO1,
-                   const GemmArgs args) {
+    gemm_tc_kernel(const __grid_constant__ TmapSet maps, const GemmArgs args) {
     using Cfg = GemmCfg<BN, EPI, NE>;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int BNH = Cfg::BNH;
@@ -277,12 +287,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
         fence_proxy_async_smem();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(&tmA);
-        prefetch_tensormap(&tmB);
-        if (EPI != EPI_CE) {
-            prefetch_tensormap(&tmO0);
-            if (EPI == EPI_GELU) prefetch_tensormap(&tmO1);
-        }
+        prefetch_tensormap(&maps.a);
+        prefetch_tensormap(&maps.b);
+        if (EPI != EPI_CE) prefetch_tensormap(&maps.o0);
+        if (EPI == EPI_GELU && args.has_out1) prefetch_tensormap(&maps.o1);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
@@ -301,14 +309,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
-            for (int u = pair; u < args.num_units && ok; u += num_pairs) {
+            const ProbInfo& p = args.pr;
+            const CUtensorMap* tmA = &maps.a;
+            const CUtensorMap* tmB = &maps.b;
+            for (int u = pair; u < p.num_units && ok; u += num_pairs) {
                 int m_blk, ucol;
-                decode_unit(args, u, m_blk, ucol);
+                decode_unit(p, u, m_blk, ucol);
                 const int n_blk0 = ucol * args.tiles_per_unit;
                 const int arow = m_blk * 2 * BM + static_cast<int>(rank) * BM;  // this CTA's A rows
                 for (int nt = 0; nt < args.tiles_per_unit && ok; ++nt) {
                     const int bcol = (n_blk0 + nt) * BN + static_cast<int>(rank) * BNH;  // this CTA's B columns
-                    for (int kb = args.kb_begin; kb < args.kb_end; ++kb) {
+                    for (int kb = p.kb_begin; kb < p.kb_end; ++kb) {
                         if (!wait_bounded(&empty_bar[stage], phase ^ 1u, ctl)) {
                             ok = false;
                             break;
@@ -317,19 +328,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                         mbar_arrive_expect_tx_cluster(full_leader, Cfg::STAGE_BYTES);
                         uint8_t* a_dst = sA + stage * Cfg::A_BYTES;
                         uint8_t* b_dst = sB + stage * Cfg::B_BYTES;
-                        if (A_MN) {
+                        if (p.a_mn) {
 #pragma unroll
                             for (int j = 0; j < BM / 64; ++j)
-                                tma_load_2d_pair(a_dst + j * 8192, &tmA, full_leader, arow + j * 64, kb * BK);
+                                tma_load_2d_pair(a_dst + j * 8192, tmA, full_leader, arow + j * 64, kb * BK);
                         } else {
-                            tma_load_2d_pair(a_dst, &tmA, full_leader, kb * BK, arow);
+                            tma_load_2d_pair(a_dst, tmA, full_leader, kb * BK, arow);
                         }
-                        if (B_MN) {
+                        if (p.b_mn) {
 #pragma unroll
                             for (int j = 0; j < BNH / 64; ++j)
-                                tma_load_2d_pair(b_dst + j * 8192, &tmB, full_leader, bcol + j * 64, kb * BK);
+                                tma_load_2d_pair(b_dst + j * 8192, tmB, full_leader, bcol + j * 64, kb * BK);
                         } else {
-                            tma_load_2d_pair(b_dst, &tmB, full_leader, kb * BK, bcol);
+                            tma_load_2d_pair(b_dst, tmB, full_leader, kb * BK, bcol);
                         }
                         if (++stage == STAGES) {
                             stage = 0;
@@ -342,12 +353,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (leader CTA) ----------------
-            constexpr uint32_t IDESC = make_idesc_bf16(2 * BM, BN, A_MN, B_MN);
             int stage = 0;
             uint32_t phase = 0;
             uint32_t tcount = 0;
             bool ok = true;
-            for (int u = pair; u < args.num_units && ok; u += num_pairs) {
+            const ProbInfo& p = args.pr;
+            const bool a_mn = p.a_mn != 0, b_mn = p.b_mn != 0;
+            for (int u = pair; u < p.num_units && ok; u += num_pairs) {
+                const uint32_t idesc = make_idesc_bf16(2 * BM, BN, a_mn, b_mn);
+                // Descriptor of a stage's first K slice; the k-th slice is that descriptor
+                // advanced in its address field (>> 4) by 2048 B (MN-major) or 32 B (K-major).
+                const uint32_t a_lbo = a_mn ? 8192u : 16u, b_lbo = b_mn ? 8192u : 16u;
+                const uint64_t a_kstep = a_mn ? (2048u >> 4) : (32u >> 4);
+                const uint64_t b_kstep = b_mn ? (2048u >> 4) : (32u >> 4);
                 for (int nt = 0; nt < args.tiles_per_unit && ok; ++nt, ++tcount) {
                     const uint32_t buf = tcount & 1u;
                     const uint32_t tph = (tcount >> 1) & 1u;
@@ -357,22 +375,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
-                    for (int kb = args.kb_begin; kb < args.kb_end; ++kb) {
+                    for (int kb = p.kb_begin; kb < p.kb_end; ++kb) {
                         if (!wait_bounded(&full_bar[stage], phase, ctl)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint32_t a_base = smem_u32(sA + stage * Cfg::A_BYTES);
-                        const uint32_t b_base = smem_u32(sB + stage * Cfg::B_BYTES);
+                        const uint64_t ad0 = make_sdesc_sw128(smem_u32(sA + stage * Cfg::A_BYTES), a_lbo, 1024);
+                        const uint64_t bd0 = make_sdesc_sw128(smem_u32(sB + stage * Cfg::B_BYTES), b_lbo, 1024);
 #pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k) {
-                            const uint64_t ad = A_MN ? make_sdesc_sw128(a_base + k * 2048, 8192, 1024)
-                                                     : make_sdesc_sw128(a_base + k * 32, 16, 1024);
-                            const uint64_t bd = B_MN ? make_sdesc_sw128(b_base + k * 2048, 8192, 1024)
-                                                     : make_sdesc_sw128(b_base + k * 32, 16, 1024);
-                            umma_bf16_pair(d_tmem, ad, bd, IDESC, (kb > args.kb_begin || k > 0) ? 1u : 0u);
-                        }
+                        for (int k = 0; k < BK / UMMA_K; ++k)
+                            umma_bf16_pair(d_tmem, ad0 + k * a_kstep, bd0 + k * b_kstep, idesc,
+                                           (kb > p.kb_begin || k > 0) ? 1u : 0u);
                         umma_commit_pair_multicast(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
                         if (++stage == STAGES) {
                             stage = 0;
@@ -399,13 +413,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
         int sbuf = 0;
         uint32_t tcount = 0;
         bool ok = true;
-        for (int u = pair; u < args.num_units && ok; u += num_pairs) {
+        const ProbInfo& p = args.pr;
+        const CUtensorMap* tmO0 = &maps.o0;
+        for (int u = pair; u < p.num_units && ok; u += num_pairs) {
             int m_blk, ucol;
-            decode_unit(args, u, m_blk, ucol);
+            decode_unit(p, u, m_blk, ucol);
             const int n_blk0 = ucol * args.tiles_per_unit;
             const int row0 = m_blk * 2 * BM + static_cast<int>(rank) * BM + q * 32;  // this warp's 32 rows
             const int row = row0 + lane;
-            const bool row_ok = row < args.M;
+            const bool row_ok = row < p.M;
             // cross-entropy running state (natural-log units)
             float run_m = -INFINITY, run_s = 0.0f, z_tgt = 0.0f;
             int tgt = -1;
@@ -429,7 +445,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                     const int c = c_begin + cc;
                     if constexpr (EPI == EPI_DGELU) {
                         const int col0 = n_blk * BN + c * 32;
-                        if (row_ok && col0 < args.N) {
+                        if (row_ok && col0 < p.N) {
                             const uint4* src = reinterpret_cast<const uint4*>(args.aux + row * args.ld_aux + col0);
 #pragma unroll
                             for (int j = 0; j < 4; ++j) {
@@ -449,34 +465,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                 auto finish = [&](int cc, const uint32_t (&r)[32], const uint32_t (&uw)[16]) {
                     const int c = c_begin + cc;
                     const int col0 = n_blk * BN + c * 32;
-                    if (col0 >= args.N) return;  // ragged N tail (whole 32-column chunks)
+                    if (col0 >= p.N) return;  // ragged N tail (whole 32-column chunks)
                     if constexpr (EPI == EPI_STORE) {
-                        uint32_t p[16];
+                        uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            p[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                        stage_and_store(&tmO0, stg, sbuf, lane, p, col0, row0);
+                            pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                        stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
                     } else if constexpr (EPI == EPI_GELU) {
-                        uint32_t p[16];
-                        if (args.out1 != nullptr) {
+                        uint32_t pk[16];
+                        if (args.has_out1) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
-                                p[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                            stage_and_store(&tmO1, stg, sbuf, lane, p, col0, row0);
+                                pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                            stage_and_store(&maps.o1, stg, sbuf, lane, pk, col0, row0);
                         }
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
-                            p[j] = pack_bf16x2(gelu_f(__uint_as_float(r[2 * j])), gelu_f(__uint_as_float(r[2 * j + 1])));
-                        stage_and_store(&tmO0, stg, sbuf, lane, p, col0, row0);
+                            pk[j] = pack_bf16x2(gelu_f(__uint_as_float(r[2 * j])), gelu_f(__uint_as_float(r[2 * j + 1])));
+                        stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
                     } else if constexpr (EPI == EPI_DGELU) {
-                        uint32_t p[16];
+                        uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const float g0 = __uint_as_float(r[2 * j]) * gelu_prime_f(bf16_lo(uw[j]));
                             const float g1 = __uint_as_float(r[2 * j + 1]) * gelu_prime_f(bf16_hi(uw[j]));
-                            p[j] = pack_bf16x2(g0, g1);
+                            pk[j] = pack_bf16x2(g0, g1);
                         }
-                        stage_and_store(&tmO0, stg, sbuf, lane, p, col0, row0);
+                        stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
                     } else {  // EPI_CE
                         const int lim = args.v_valid - col0;  // valid columns in this chunk
                         if (lim > 0) {
@@ -532,10 +548,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
             if (!ok) break;
             if constexpr (EPI == EPI_CE) {
                 if (row_ok) {
-                    float* w = args.ws + static_cast<long long>(ucol) * 3 * args.M;
+                    float* w = args.ws + static_cast<long long>(ucol) * 3 * p.M;
                     w[row] = run_m;
-                    w[args.M + row] = run_s;
-                    w[2 * args.M + row] = z_tgt;
+                    w[p.M + row] = run_s;
+                    w[2 * p.M + row] = z_tgt;
                 }
             }
         }
@@ -562,7 +578,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
 }
 
 // Number of CTA pairs that can be resident at once for one kernel instantiation.
-template <int BN, bool A_MN, bool B_MN, int EPI, int NE>
+template <int BN, int EPI, int NE>
 inline int resident_pairs(int num_sms) {
     using Cfg = GemmCfg<BN, EPI, NE>;
     static int cached[64] = {0};
@@ -574,7 +590,7 @@ inline int resident_pairs(int num_sms) {
     cfg.blockDim = dim3(Cfg::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<BN, A_MN, B_MN, EPI, NE>, &cfg) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_tc_kernel<BN, EPI, NE>, &cfg) != cudaSuccess ||
         clusters <= 0) {
         cudaGetLastError();
         clusters = num_sms / 2;
@@ -585,18 +601,17 @@ inline int resident_pairs(int num_sms) {
 }
 
 // Host-side launcher: grid = 2 x min(units, resident pairs), one CTA per SM.
-template <int BN, bool A_MN, bool B_MN, int EPI, int NE>
-inline cudaError_t launch_gemm_tc(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmO0,
-                                  const CUtensorMap& tmO1, const GemmArgs& args, int num_sms, cudaStream_t stream) {
+template <int BN, int EPI, int NE>
+inline cudaError_t launch_gemm_tc(const TmapSet& maps, const GemmArgs& args, int num_sms, cudaStream_t stream) {
     using Cfg = GemmCfg<BN, EPI, NE>;
-    auto kern = gemm_tc_kernel<BN, A_MN, B_MN, EPI, NE>;
+    auto kern = gemm_tc_kernel<BN, EPI, NE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    const int pairs = resident_pairs<BN, A_MN, B_MN, EPI, NE>(num_sms);
-    const int use = args.num_units < pairs ? args.num_units : pairs;
+    const int pairs = resident_pairs<BN, EPI, NE>(num_sms);
+    const int use = args.pr.num_units < pairs ? args.pr.num_units : pairs;
     if (use <= 0) return cudaSuccess;
-    kern<<<2 * use, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(tmA, tmB, tmO0, tmO1, args);
+    kern<<<2 * use, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(maps, args);
     return cudaGetLastError();
 }
 

@@ -21,18 +21,26 @@ static mp_status check_mlp_shape(int T, int h, int f, int t) {
     return MP_OK;
 }
 
-// a_bytes / b_bytes: sizes of the A (M side) and B (N side) operands, for the unit order.
-static GemmArgs base_args(int M, int N, int bn, int kb_begin, int kb_end, double a_bytes, double b_bytes,
-                          uint32_t* status) {
+// One GEMM of a launch: C[M, N] over K blocks [kb_begin, kb_end). a_bytes / b_bytes
+// are the sizes of the A (M side) and B (N side) operands, for the unit order.
+static ProbInfo problem(int M, int N, int bn, int kb_begin, int kb_end, bool a_mn, bool b_mn, double a_bytes,
+                        double b_bytes) {
+    ProbInfo p{};
+    p.M = M;
+    p.N = N;
+    p.num_m_blocks = ceil_div(M, 2 * BM);  // 256-row blocks: one per CTA-pair tile
+    p.num_units = p.num_m_blocks * ceil_div(N, bn);
+    p.n_fastest = n_fastest_order(a_bytes, b_bytes);
+    p.kb_begin = kb_begin;
+    p.kb_end = kb_end;
+    p.a_mn = a_mn ? 1 : 0;
+    p.b_mn = b_mn ? 1 : 0;
+    return p;
+}
+
+static GemmArgs launch_args(uint32_t* status) {
     GemmArgs a{};
-    a.M = M;
-    a.N = N;
-    a.num_m_blocks = ceil_div(M, 2 * BM);  // 256-row blocks: one per CTA-pair tile
     a.tiles_per_unit = 1;
-    a.num_units = a.num_m_blocks * ceil_div(N, bn);
-    a.n_fastest = n_fastest_order(a_bytes, b_bytes);
-    a.kb_begin = kb_begin;
-    a.kb_end = kb_end;
     a.status = status;
     a.budget_ns = wait_budget_ns();
     return a;
@@ -54,32 +62,29 @@ extern "C" mp_status mp_mlp_fwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
     int sms = 0;
     if ((st = check_device(&sms)) != MP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-
     const double Tb = 2.0 * T, hb = 2.0 * h;
-    CUtensorMap tmX, tmA, tmY, tmB, tmYo, tmUo, tmZo;
-    if (!make_tmap_bf16(&tmX, X, h, T, h, 64, BM) || !make_tmap_bf16(&tmA, A, f, h, f, 64, 64) ||
-        !make_tmap_bf16(&tmY, Y, f, T, f, 64, BM) || !make_tmap_bf16(&tmB, B, h, f, h, 64, 64) ||
-        !make_tmap_bf16_out(&tmYo, Y, f, T, f) || !make_tmap_bf16_out(&tmZo, Z, h, T, h) ||
-        !make_tmap_bf16_out(&tmUo, U_save ? static_cast<const void*>(U_save) : static_cast<const void*>(Y), f, T, f))
-        return MP_ERR_CUDA;
 
-    // K1: column-parallel GEMM + GeLU over all shards' columns.
-    GemmArgs a1 = base_args(T, f, 256, 0, h / BK, Tb * h, hb * f, d_status);
-    a1.out0 = reinterpret_cast<__nv_bfloat16*>(Y);
-    a1.ld0 = f;
-    a1.out1 = reinterpret_cast<__nv_bfloat16*>(U_save);
-    a1.ld1 = f;
-    if (launch_gemm_tc<256, false, true, EPI_GELU, 8>(tmX, tmA, tmYo, tmUo, a1, sms, s) != cudaSuccess)
+    // K1: column-parallel GEMM + GeLU over all shards' columns: U = X A (A MN-major), Y = GeLU(U).
+    TmapSet m1{};
+    if (!make_tmap_bf16(&m1.a, X, h, T, h, 64, BM) || !make_tmap_bf16(&m1.b, A, f, h, f, 64, 64) ||
+        !make_tmap_bf16_out(&m1.o0, Y, f, T, f) ||
+        (U_save && !make_tmap_bf16_out(&m1.o1, U_save, f, T, f)))
         return MP_ERR_CUDA;
+    GemmArgs a1 = launch_args(d_status);
+    a1.pr = problem(T, f, 256, 0, h / BK, false, true, Tb * h, hb * f);
+    a1.has_out1 = U_save ? 1 : 0;
+    if (launch_gemm_tc<256, EPI_GELU, 8>(m1, a1, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
-    // K2: row-parallel GEMM; K blocks of shard i are [i*f/t, (i+1)*f/t) / BK, visited
-    // for i = 0..t-1 in order, all into the same accumulator (the g sum).
+    // K2: row-parallel GEMM Z = sum_i Y_i B_i; K blocks of shard i are [i*f/t, (i+1)*f/t) / BK,
+    // visited for i = 0..t-1 in order, all into the same accumulator (the g sum).
     const int fs = f / t;
-    GemmArgs a2 = base_args(T, h, 256, 0 * (fs / BK), t * (fs / BK), Tb * f, hb * f, d_status);
-    a2.out0 = reinterpret_cast<__nv_bfloat16*>(Z);
-    a2.ld0 = h;
-    if (launch_gemm_tc<256, false, true, EPI_STORE, 4>(tmY, tmB, tmZo, tmZo, a2, sms, s) != cudaSuccess)
+    TmapSet m2{};
+    if (!make_tmap_bf16(&m2.a, Y, f, T, f, 64, BM) || !make_tmap_bf16(&m2.b, B, h, f, h, 64, 64) ||
+        !make_tmap_bf16_out(&m2.o0, Z, h, T, h))
         return MP_ERR_CUDA;
+    GemmArgs a2 = launch_args(d_status);
+    a2.pr = problem(T, h, 256, 0 * (fs / BK), t * (fs / BK), false, true, Tb * f, hb * f);
+    if (launch_gemm_tc<256, EPI_STORE, 4>(m2, a2, sms, s) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
 
@@ -104,57 +109,46 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
             return MP_ERR_CUDA;
         return MP_OK;
     }
+    const double Tb = 2.0 * T, hb = 2.0 * h, fb = 2.0 * f;
 
     // K3: dU = (dZ B^T) * GeLU'(U).  A operand dZ [T,h] (K-major), B operand B [f,h] (K-major).
-    const double Tb = 2.0 * T, hb = 2.0 * h, fb = 2.0 * f;
-    CUtensorMap tm_dZ_k, tm_B_k, tm_dU_o;
-    if (!make_tmap_bf16(&tm_dZ_k, dZ, h, T, h, 64, BM) || !make_tmap_bf16(&tm_B_k, B, h, f, h, 64, 128) ||
-        !make_tmap_bf16_out(&tm_dU_o, dU_ws, f, T, f))
+    TmapSet m3{};
+    if (!make_tmap_bf16(&m3.a, dZ, h, T, h, 64, BM) || !make_tmap_bf16(&m3.b, B, h, f, h, 64, 128) ||
+        !make_tmap_bf16_out(&m3.o0, dU_ws, f, T, f))
         return MP_ERR_CUDA;
-    GemmArgs a3 = base_args(T, f, 256, 0, h / BK, Tb * h, fb * h, d_status);
-    a3.out0 = reinterpret_cast<__nv_bfloat16*>(dU_ws);
-    a3.ld0 = f;
+    GemmArgs a3 = launch_args(d_status);
+    a3.pr = problem(T, f, 256, 0, h / BK, false, false, Tb * h, fb * h);
     a3.aux = reinterpret_cast<const __nv_bfloat16*>(U);
     a3.ld_aux = f;
-    if (launch_gemm_tc<256, false, false, EPI_DGELU, 8>(tm_dZ_k, tm_B_k, tm_dU_o, tm_dU_o, a3, sms, s) !=
-        cudaSuccess)
-        return MP_ERR_CUDA;
+    if (launch_gemm_tc<256, EPI_DGELU, 8>(m3, a3, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
-    // K4: dX = sum_i dU_i A_i^T.  A operand dU [T,f] (K-major), B operand A [h,f] (K-major).
-    CUtensorMap tm_dU_k, tm_A_k, tm_dX_o;
-    if (!make_tmap_bf16(&tm_dU_k, dU_ws, f, T, f, 64, BM) || !make_tmap_bf16(&tm_A_k, A, f, h, f, 64, 128) ||
-        !make_tmap_bf16_out(&tm_dX_o, dX, h, T, h))
-        return MP_ERR_CUDA;
+    // K4: dX = sum_i dU_i A_i^T.  A operand dU [T,f] (K-major), B operand A [h,f] (K-major); K blocks of
+    // shard i are [i*f/t, (i+1)*f/t) / BK, visited for i = 0..t-1 in order (the f sum).
     const int fs = f / t;
-    GemmArgs a4 = base_args(T, h, 256, 0 * (fs / BK), t * (fs / BK), Tb * f, hb * f, d_status);
-    a4.out0 = reinterpret_cast<__nv_bfloat16*>(dX);
-    a4.ld0 = h;
-    if (launch_gemm_tc<256, false, false, EPI_STORE, 4>(tm_dU_k, tm_A_k, tm_dX_o, tm_dX_o, a4, sms, s) !=
-        cudaSuccess)
+    TmapSet m4{};
+    if (!make_tmap_bf16(&m4.a, dU_ws, f, T, f, 64, BM) || !make_tmap_bf16(&m4.b, A, f, h, f, 64, 128) ||
+        !make_tmap_bf16_out(&m4.o0, dX, h, T, h))
         return MP_ERR_CUDA;
+    GemmArgs a4 = launch_args(d_status);
+    a4.pr = problem(T, h, 256, 0 * (fs / BK), t * (fs / BK), false, false, Tb * f, hb * f);
+    if (launch_gemm_tc<256, EPI_STORE, 4>(m4, a4, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
     // K5a: dA = X^T dU (M = h, N = f, K = T).  Both operands MN-major.
-    CUtensorMap tm_X_mn, tm_dU_mn, tm_dA_o;
-    if (!make_tmap_bf16(&tm_X_mn, X, h, T, h, 64, 64) || !make_tmap_bf16(&tm_dU_mn, dU_ws, f, T, f, 64, 64) ||
-        !make_tmap_bf16_out(&tm_dA_o, dA, f, h, f))
+    TmapSet m5{};
+    if (!make_tmap_bf16(&m5.a, X, h, T, h, 64, 64) || !make_tmap_bf16(&m5.b, dU_ws, f, T, f, 64, 64) ||
+        !make_tmap_bf16_out(&m5.o0, dA, f, h, f))
         return MP_ERR_CUDA;
-    GemmArgs a5 = base_args(h, f, 256, 0, ceil_div(T, BK), Tb * h, Tb * f, d_status);
-    a5.out0 = reinterpret_cast<__nv_bfloat16*>(dA);
-    a5.ld0 = f;
-    if (launch_gemm_tc<256, true, true, EPI_STORE, 4>(tm_X_mn, tm_dU_mn, tm_dA_o, tm_dA_o, a5, sms, s) !=
-        cudaSuccess)
-        return MP_ERR_CUDA;
+    GemmArgs a5 = launch_args(d_status);
+    a5.pr = problem(h, f, 256, 0, ceil_div(T, BK), true, true, Tb * h, Tb * f);
+    if (launch_gemm_tc<256, EPI_STORE, 4>(m5, a5, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
     // K5b: dB = Y^T dZ (M = f, N = h, K = T).  Both operands MN-major.
-    CUtensorMap tm_Y_mn, tm_dZ_mn, tm_dB_o;
-    if (!make_tmap_bf16(&tm_Y_mn, Y, f, T, f, 64, 64) || !make_tmap_bf16(&tm_dZ_mn, dZ, h, T, h, 64, 64) ||
-        !make_tmap_bf16_out(&tm_dB_o, dB, h, f, h))
+    TmapSet m6{};
+    if (!make_tmap_bf16(&m6.a, Y, f, T, f, 64, 64) || !make_tmap_bf16(&m6.b, dZ, h, T, h, 64, 64) ||
+        !make_tmap_bf16_out(&m6.o0, dB, h, f, h))
         return MP_ERR_CUDA;
-    GemmArgs a6 = base_args(f, h, 256, 0, ceil_div(T, BK), Tb * f, Tb * h, d_status);
-    a6.out0 = reinterpret_cast<__nv_bfloat16*>(dB);
-    a6.ld0 = h;
-    if (launch_gemm_tc<256, true, true, EPI_STORE, 4>(tm_Y_mn, tm_dZ_mn, tm_dB_o, tm_dB_o, a6, sms, s) !=
-        cudaSuccess)
-        return MP_ERR_CUDA;
+    GemmArgs a6 = launch_args(d_status);
+    a6.pr = problem(f, h, 256, 0, ceil_div(T, BK), true, true, Tb * f, Tb * h);
+    if (launch_gemm_tc<256, EPI_STORE, 4>(m6, a6, sms, s) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
