@@ -440,6 +440,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("mptp", "reference"), default="mptp")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time MLP fwd+bwd and the fused CE at every point of the layer sweep (one JSON line each)")
     ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "mlp"), default="none",
                     help="run only a small case of one entry point a few times (for ncu), print nothing")
     args = ap.parse_args(argv)
@@ -463,6 +465,8 @@ def main(argv=None):
 
     if args.profile_case != "none":
         return profile_case(args.profile_case, dev)
+    if args.sweep:
+        return run_sweep(dev, max(args.steps // 20, 5), args.warmup)
 
     step = Step(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -535,6 +539,61 @@ def main(argv=None):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+    return 0
+
+
+def run_sweep(dev, reps, warmup):
+    """MLP fwd+bwd and fused CE throughput at every sweep point: h in {1536, 1920, 2304,
+    3072} (f = 4h), T in {2048, 8192}, t in {1, 2, 4, 8}, vocabulary 51,200 (50,257
+    valid). Median of `reps` launches, L2 flushed before each."""
+    import torch
+
+    import synth
+    import tensor_transformer_layer_gb300 as mp
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def med(fn):
+        for _ in range(warmup):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ts.sort()
+        return ts[len(ts) // 2]
+
+    for h in (1536, 1920, 2304, 3072):
+        f = 4 * h
+        for T in (2048, 8192):
+            mi = synth.mlp_inputs(T, h, f, seed=1004)
+            d = {k: v.to(dev) for k, v in mi.items()}
+            e = lambda *s_: torch.empty(*s_, dtype=torch.bfloat16, device=dev)
+            Z, Y, U, dX, dA, dB, dU = e(T, h), e(T, f), e(T, f), e(T, h), e(h, f), e(f, h), e(T, f)
+            ci = synth.ce_inputs(T, h, 51200, 50257, seed=1004)
+            Xc, E, tg = ci["X"].to(dev), ci["E"].to(dev), ci["target"].to(dev)
+            loss = torch.empty(T, dtype=torch.float32, device=dev)
+            for t in (1, 2, 4, 8):
+                ms = med(lambda: (mp.mp_mlp_fwd(d["X"], d["A"], d["B"], Z, Y, U, t=t),
+                                  mp.mp_mlp_bwd(d["X"], d["A"], d["B"], U, Y, d["dZ"], dX, dA, dB, dU, t=t)))
+                ws = torch.empty(mp.mp_vocab_ce_workspace_bytes(T, 51200, t), dtype=torch.uint8, device=dev)
+                ce_ms = med(lambda: mp.mp_vocab_ce(Xc, E, tg, loss, ws, v_valid=50257, t=t))
+                mlp_tf = 12.0 * T * h * f / (ms * 1e-3) / 1e12
+                ce_tf = 2.0 * T * h * 51200 / (ce_ms * 1e-3) / 1e12
+                print(json.dumps({
+                    "sweep": True, "h": h, "f": f, "T": T, "t": t, "heads": h // 96,
+                    "mlp_fwd_bwd_ms": ms, "mlp_tflops": mlp_tf,
+                    "ce_ms": ce_ms, "ce_tflops": ce_tf, "ce_tokens_per_s": T / (ce_ms * 1e-3),
+                    "pct_of_measured_bf16_sustained": {"mlp": mlp_tf / peaks["bf16_tflops_sustained"],
+                                                       "ce": ce_tf / peaks["bf16_tflops_sustained"]},
+                    "peak_source": peak_src}), flush=True)
+            del d, Z, Y, U, dX, dA, dB, dU, Xc, E, tg
+            torch.cuda.empty_cache()
     return 0
 
 
