@@ -19,6 +19,10 @@ definition states. Sources, cited by page title and section:
 [p5] "Megatron-LM, annotated" (ai-primer), §2.2 (GELU, erf form), §3.1 (the
      two-token MLP example), §3.4 (embedding, loss, vocabulary padding).
 
+The cross-entropy backward (``ce_bwd``) is not spelled out on the pages, which
+train the model but describe only the forward fusion; it is the plain derivative
+of the softmax cross-entropy, pinned by finite differences.
+
 Pins (tests marked "not gpu"): GELU values printed in [p5] §2.2, the [p5] §3.1
 worked example and its wrong row cut, closed forms of GELU, finite differences
 of the backward, brute-force softmax cross-entropy on tiny vocabularies, the
@@ -36,13 +40,15 @@ from .mlp import (
     mlp_fwd_rows,
     mlp_bwd_sampled,
 )
-from .ce import ce_loss, ce_partition_triples, ce_combine, ce_loss_partitioned
+from .ce import (ce_loss, ce_partition_triples, ce_combine, ce_loss_partitioned, ce_bwd, ce_logsumexp,
+                 ce_bwd_sampled)
 from .padding import pad_vocab
 
 __all__ = [
     "gelu", "gelu_prime", "std_normal_cdf", "std_normal_pdf",
     "mlp_fwd", "mlp_bwd", "mlp_sharded_fwd", "mlp_sharded_bwd", "first_layer_row_cut",
     "mlp_fwd_rows", "mlp_bwd_sampled",
-    "ce_loss", "ce_partition_triples", "ce_combine", "ce_loss_partitioned",
+    "ce_loss", "ce_partition_triples", "ce_combine", "ce_loss_partitioned", "ce_bwd", "ce_logsumexp",
+    "ce_bwd_sampled",
     "pad_vocab",
 ]

@@ -83,3 +83,67 @@ def ce_combine(m, s, zt):
 
 def ce_loss_partitioned(X, E, target, v_valid: int, P: int):
     return ce_combine(*ce_partition_triples(X, E, target, v_valid, P))
+
+
+def ce_bwd(X, E, target, dloss, v_valid: int):
+    """Gradient of sum_r dloss[r] * loss[r] (loss as in ``ce_loss``) w.r.t. X and E.
+
+    The plain derivative of softmax cross-entropy: with p = softmax(z) over the
+    valid columns, dZ[r, c] = dloss[r] * (p[r, c] - [c == target[r]]);
+    dX = dZ E[:v_valid]; dE[:v_valid] = dZ^T X and dE[v_valid:] = 0 (padding rows
+    take no part in the loss). Returns dict with dX, dE, dZ.
+    """
+    X, E = _f64(X), _f64(E)
+    target = np.asarray(target, dtype=np.int64)
+    dloss = _f64(dloss)
+    if np.any(target < 0) or np.any(target >= v_valid):
+        raise ValueError("target id outside [0, v_valid)")
+    z = X @ E[:v_valid].T
+    M = z.max(axis=1, keepdims=True)
+    p = np.exp(z - M)
+    p /= p.sum(axis=1, keepdims=True)
+    p[np.arange(z.shape[0]), target] -= 1.0
+    dZ = dloss[:, None] * p
+    dE = np.zeros_like(E)
+    dE[:v_valid] = dZ.T @ X
+    return {"dX": dZ @ E[:v_valid], "dE": dE, "dZ": dZ}
+
+
+def ce_logsumexp(X, E, v_valid: int, block: int = 512):
+    """Per-token log sum_c exp(z[r, c]) over the valid columns, computed a block of
+    tokens at a time (same arithmetic as ``ce_loss``, bounded memory)."""
+    X, E = _f64(X), _f64(E)
+    out = np.empty(X.shape[0])
+    Ev = E[:v_valid]
+    for lo in range(0, X.shape[0], block):
+        z = X[lo:lo + block] @ Ev.T
+        M = z.max(axis=1)
+        out[lo:lo + block] = M + np.log(np.exp(z - M[:, None]).sum(axis=1))
+    return out
+
+
+def ce_bwd_sampled(X, E, target, dloss, v_valid: int, rows, e_rows, lse=None):
+    """dX[rows] and dE[e_rows] of ``ce_bwd`` without forming the full [T, v] matrix.
+
+    A row of dX needs its token's logits over the vocabulary; a row c of dE needs
+    column c of dZ over all tokens, i.e. z[:, c] and every token's log-sum-exp
+    (``lse``, computed here by ``ce_logsumexp`` when not given).
+    """
+    X, E = _f64(X), _f64(E)
+    target = np.asarray(target, dtype=np.int64)
+    dloss = _f64(dloss)
+    rows = np.asarray(rows)
+    e_rows = np.asarray(e_rows)
+    r = ce_bwd(X[rows], E, target[rows], dloss[rows], v_valid)
+    if lse is None:
+        lse = ce_logsumexp(X, E, v_valid)
+    dE = np.zeros((len(e_rows), E.shape[1]))
+    valid = e_rows < v_valid
+    if np.any(valid):
+        c = e_rows[valid]
+        zc = X @ E[c].T                                   # [T, n]
+        dZc = np.exp(zc - lse[:, None])
+        dZc -= (target[:, None] == c[None, :])
+        dZc *= dloss[:, None]
+        dE[valid] = dZc.T @ X
+    return {"dX_rows": r["dX"], "dE_rows": dE}
