@@ -290,6 +290,40 @@ def time_breakdown(step, reps, flush):
     return out
 
 
+def time_next_rows(step, reps, flush):
+    """Rows beyond the step (measured beside it, not inside `value`): the fused
+    vocab-parallel cross-entropy backward on the step's CE workload."""
+    import torch
+    mp, d = step.mp, step.d
+    T, h, v_pad, v_valid, t = CE["T"], CE["h"], CE["v_pad"], CE["v_valid"], CE["t"]
+    dloss = torch.full((T,), 1.0 / T, dtype=torch.float32, device=d["Xc"].device)
+    dXc = torch.empty(T, h, dtype=torch.bfloat16, device=d["Xc"].device)
+    dE = torch.empty(v_pad, h, dtype=torch.bfloat16, device=d["Xc"].device)
+    wsb = torch.empty(mp.mp_vocab_ce_bwd_workspace_bytes(T, h, v_pad, t), dtype=torch.uint8, device=d["Xc"].device)
+    mp.mp_vocab_ce(d["Xc"], d["E"], d["target"], d["loss"], step.ws, v_valid=v_valid, t=t)
+    fn = lambda: mp.mp_vocab_ce_bwd(d["Xc"], d["E"], d["target"], d["loss"], dloss, dXc, dE, wsb, v_valid=v_valid,
+                                    t=t, d_status=step.status)
+    fn()
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    ts.sort()
+    ms = ts[len(ts) // 2]
+    step.check_status()
+    algo = 4.0 * T * h * v_pad      # dX = dZ E and dE = dZ^T X
+    executed = 6.0 * T * h * v_pad  # plus the logit recompute (logits are never stored)
+    return {"ce_bwd": {"ms": ms, "tflops_algorithmic": algo / (ms * 1e-3) / 1e12,
+                       "tflops_executed": executed / (ms * 1e-3) / 1e12, "tokens_per_s": T / (ms * 1e-3),
+                       "launches": 1 + 3 * t,
+                       "flop_note": "algorithmic 4*T*h*v_pad (dX, dE); executed adds the 2*T*h*v_pad recompute"}}
+
+
 def time_e2e(step, steps, warmup):
     """The step through the same C-ABI calls with every input copied in from pinned host
     memory and every result (Z, dX, dA, dB, loss) copied back, all inside the timed
@@ -490,6 +524,7 @@ def main(argv=None):
     value = world * step_flop() * args.steps / (total_ms * 1e-3) / 1e12
 
     breakdown = time_breakdown(step, 9, flush)
+    next_rows = time_next_rows(step, 9, flush)
     peaks, peak_src = load_peaks()
     ce_avg_ms = sum(ce_ms) / len(ce_ms)
     ce_achieved = ce_flop() / (ce_avg_ms * 1e-3) / 1e12
@@ -525,6 +560,7 @@ def main(argv=None):
             "ce_tokens_per_s": CE["T"] / ((breakdown["ce_partials"] + breakdown["ce_combine"]) * 1e-3),
             "ce_tflops": ce_flop() / ((breakdown["ce_partials"] + breakdown["ce_combine"]) * 1e-3) / 1e12,
             "breakdown_ms": breakdown,
+            "next_rows": next_rows,
             "roofline": {"kernel": "mp_vocab_ce_partials (logit GEMM + online LSE epilogue)", "bound": "tensor",
                          "achieved": ce_achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                          "frac": ce_achieved / peaks["bf16_tflops_sustained"],

@@ -157,6 +157,32 @@ MP_API mp_status mp_vocab_ce_combine(const void* workspace, size_t workspace_byt
                               uint32_t* d_status, void* stream);
 
 /*
+ * Backward of the vocab-parallel cross-entropy. The pages describe the fused
+ * forward only; this is the plain derivative of softmax cross-entropy, computed
+ * in the forward's vocabulary partition so that logit gradients exist for one
+ * shard (v_pad / t columns) at a time:
+ *   dZ[r, c] = dloss[r] * (softmax(z[r])_c - [c == target[r]]) for c < v_valid,
+ *   0 for padding columns;  dX = dZ E;  dE = dZ^T X  (padding rows of dE are 0).
+ * The per-token log-sum-exp is taken from the forward's loss:
+ *   lse[r] = loss[r] + X[r] . E[target[r]].
+ *
+ *   X [T, h] bf16, E [v_pad, h] bf16, target [T] int32, loss [T] fp32 (the output of
+ *   mp_vocab_ce on the same X, E, target), dloss [T] fp32 (upstream gradient, e.g.
+ *   1/T for a mean) -> dX [T, h] bf16, dE [v_pad, h] bf16 (overwritten).
+ *   workspace >= mp_vocab_ce_bwd_workspace_bytes(T, h, v_pad, t) bytes: the
+ *   log-sum-exp [T], an fp32 dX accumulator [T, h] and one shard of dZ [T, v_pad/t].
+ *   Size rules as mp_vocab_ce. A target outside [0, v_valid) sets
+ *   MP_DEV_TARGET_RANGE and contributes no gradient. dX accumulates the shards in
+ *   ascending order (deterministic).
+ */
+MP_API size_t mp_vocab_ce_bwd_workspace_bytes(int T, int h, int v_pad, int t);
+MP_API mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const int32_t* target,
+                          const float* loss, const float* dloss,
+                          mp_bf16* dX, mp_bf16* dE, void* workspace, size_t workspace_bytes,
+                          int T, int h, int v_pad, int v_valid, int t,
+                          uint32_t* d_status, void* stream);
+
+/*
  * mp_vocab_ce for callers that cannot allocate device memory. The paper has no
  * counterpart to this entry point; it exists for callers whose device memory is
  * owned by another pool (a serving runtime that reserves HBM at start-up and

@@ -32,7 +32,7 @@ STATUS_NAMES = {
 # Every symbol include/mptp.h declares.
 EXPORTS = ("mp_mlp_fwd", "mp_mlp_bwd", "mp_vocab_ce_workspace_bytes", "mp_vocab_ce", "mp_vocab_ce_partials",
            "mp_vocab_ce_combine", "mp_status_string", "mp_status_from_device", "mp_version",
-           "mp_vocab_ce_noalloc")
+           "mp_vocab_ce_noalloc", "mp_vocab_ce_bwd_workspace_bytes", "mp_vocab_ce_bwd")
 
 
 class MptpError(RuntimeError):
@@ -66,6 +66,10 @@ def lib() -> ctypes.CDLL:
         L.mp_vocab_ce_partials.restype = _I
         L.mp_vocab_ce_combine.argtypes = [_P, ctypes.c_size_t, _P, _P, _I, _I, _I, _I, _P, _P]
         L.mp_vocab_ce_combine.restype = _I
+        L.mp_vocab_ce_bwd_workspace_bytes.argtypes = [_I, _I, _I, _I]
+        L.mp_vocab_ce_bwd_workspace_bytes.restype = ctypes.c_size_t
+        L.mp_vocab_ce_bwd.argtypes = [_P] * 7 + [_P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P, _P]
+        L.mp_vocab_ce_bwd.restype = _I
         L.mp_vocab_ce_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]
         L.mp_vocab_ce_noalloc.restype = _I
         L.mp_status_string.argtypes = [_I]
@@ -201,6 +205,25 @@ def mp_vocab_ce_noalloc(X, E, target, loss, *, v_valid: int, t: int, d_status=No
         _ptr(target, "target", dtype=torch.int32, shape=(T,)), _ptr(loss, "loss", dtype=torch.float32, shape=(T,)),
         T, h, v_pad, int(v_valid), int(t), _status_ptr(d_status), _stream(stream))
     _check("mp_vocab_ce_noalloc", code)
+
+
+def mp_vocab_ce_bwd_workspace_bytes(T: int, h: int, v_pad: int, t: int) -> int:
+    return int(lib().mp_vocab_ce_bwd_workspace_bytes(int(T), int(h), int(v_pad), int(t)))
+
+
+def mp_vocab_ce_bwd(X, E, target, loss, dloss, dX, dE, workspace, *, v_valid: int, t: int, d_status=None,
+                    stream=None) -> None:
+    """Backward of the fused vocab-parallel cross-entropy: dX [T,h], dE [v_pad,h] (bf16)."""
+    T, h = X.shape
+    v_pad = E.shape[0]
+    wp, wb = _ws(workspace)
+    code = lib().mp_vocab_ce_bwd(
+        _ptr(X, "X", shape=(T, h)), _ptr(E, "E", shape=(v_pad, h)),
+        _ptr(target, "target", dtype=torch.int32, shape=(T,)), _ptr(loss, "loss", dtype=torch.float32, shape=(T,)),
+        _ptr(dloss, "dloss", dtype=torch.float32, shape=(T,)), _ptr(dX, "dX", shape=(T, h)),
+        _ptr(dE, "dE", shape=(v_pad, h)), wp, wb, T, h, v_pad, int(v_valid), int(t), _status_ptr(d_status),
+        _stream(stream))
+    _check("mp_vocab_ce_bwd", code)
 
 
 def mp_status_from_device(bits: int) -> int:

@@ -1,0 +1,189 @@
+// Entry point of the vocab-parallel cross-entropy backward: mp_vocab_ce_bwd.
+//
+// The pages describe the fused forward only ("Megatron-LM: Training Multi-Billion
+// Parameter Language Models Using Model Parallelism", section 3.4, "Output Embedding
+// Parallelism and the Fused Cross-Entropy Optimization"); the backward is the plain
+// derivative of softmax cross-entropy: dZ = dloss * (softmax(z) - onehot(target)),
+// dX = dZ E, dE = dZ^T X. It keeps the forward's vocabulary partition: for shard i
+// (rows [i v_pad/t, (i+1) v_pad/t) of E), in ascending order,
+//   K10  z_i = X E_i^T recomputed; the epilogue turns it into dZ_i (bf16) from the
+//        per-token log-sum-exp, so only one shard of logit gradients exists at a time;
+//   K11  dE_i = dZ_i^T X  (both operands MN-major);
+//   K12  dX += dZ_i E_i   (fp32 accumulation across shards in shard order - the sum the
+//        forward's all-reduce would carry - and one bf16 store after the last shard).
+// The log-sum-exp comes from the forward's loss: lse = loss + z_target, with z_target
+// = X[r] . E[target[r]] recomputed in fp32 (K9).
+#include "mptp_gemm.cuh"
+#include "mptp_internal.h"
+
+namespace mptp {
+
+// One warp per token: lse[r] = loss[r] + X[r] . E[target[r]] (fp32 accumulation of
+// bf16 products); NaN and MP_DEV_TARGET_RANGE for a target outside [0, v_valid).
+__global__ void __launch_bounds__(256) ce_lse_kernel(const __nv_bfloat16* __restrict__ X,
+                                                     const __nv_bfloat16* __restrict__ E,
+                                                     const int32_t* __restrict__ target,
+                                                     const float* __restrict__ loss, float* __restrict__ lse, int T,
+                                                     int h, int v_valid, uint32_t* status) {
+    const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= T) return;
+    const int tg = target[r];
+    if (tg < 0 || tg >= v_valid) {
+        if (lane == 0) {
+            lse[r] = __int_as_float(0x7fc00000);
+            if (status) atomicOr(status, DEV_TARGET_RANGE);
+        }
+        return;
+    }
+    const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<long long>(r) * h);
+    const uint4* er = reinterpret_cast<const uint4*>(E + static_cast<long long>(tg) * h);
+    float acc = 0.0f;
+    for (int i = lane; i < h / 8; i += 32) {
+        const uint4 a = xr[i], b = er[i];
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            acc = fmaf(bf16_lo(aw[j]), bf16_lo(bw[j]), acc);
+            acc = fmaf(bf16_hi(aw[j]), bf16_hi(bw[j]), acc);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) lse[r] = loss[r] + acc;
+}
+
+struct CeBwdLayout {
+    size_t lse_off, acc_off, dz_off, total;
+};
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+static bool ce_bwd_layout(int T, int h, int v_pad, int t, CeBwdLayout* L) {
+    if (T < 0 || h <= 0 || t < 1 || v_pad <= 0 || v_pad % (128 * t) != 0) return false;
+    const size_t vs = static_cast<size_t>(v_pad / t);
+    L->lse_off = 0;
+    L->acc_off = align256(size_t(T) * 4);
+    L->dz_off = L->acc_off + align256(size_t(T) * h * 4);
+    L->total = L->dz_off + align256(size_t(T) * vs * 2);
+    return true;
+}
+
+}  // namespace mptp
+
+using namespace mptp;
+
+extern "C" size_t mp_vocab_ce_bwd_workspace_bytes(int T, int h, int v_pad, int t) {
+    CeBwdLayout L;
+    if (!ce_bwd_layout(T, h, v_pad, t, &L)) return 0;
+    return L.total;
+}
+
+extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const int32_t* target, const float* loss,
+                                     const float* dloss, mp_bf16* dX, mp_bf16* dE, void* workspace,
+                                     size_t workspace_bytes, int T, int h, int v_pad, int v_valid, int t,
+                                     uint32_t* d_status, void* stream) {
+    if (T < 0 || h <= 0 || v_pad <= 0 || t < 1 || v_valid < 1) return MP_ERR_INVALID_ARG;
+    if (h % 64 != 0 || v_pad % (128 * t) != 0 || v_valid > v_pad) return MP_ERR_UNSUPPORTED_SHAPE;
+    if (!E || !dE) return MP_ERR_INVALID_ARG;
+    if (T > 0 && (!X || !target || !loss || !dloss || !dX || !workspace)) return MP_ERR_INVALID_ARG;
+    const void* ptrs[] = {X, E, target, loss, dloss, dX, dE, workspace};
+    for (const void* p : ptrs)
+        if (p && !aligned16(p)) return MP_ERR_MISALIGNED;
+    if (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)) return MP_ERR_MISALIGNED;
+    CeBwdLayout lay;
+    ce_bwd_layout(T, h, v_pad, t, &lay);
+    if (T > 0 && workspace_bytes < lay.total) return MP_ERR_WORKSPACE;
+    int sms = 0;
+    mp_status st = check_device(&sms);
+    if (st != MP_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        // No tokens: the embedding gradient is a sum over zero tokens.
+        return cudaMemsetAsync(dE, 0, size_t(v_pad) * h * 2, s) == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+    }
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* lse = reinterpret_cast<float*>(ws + lay.lse_off);
+    float* acc = reinterpret_cast<float*>(ws + lay.acc_off);
+    __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + lay.dz_off);
+    const __nv_bfloat16* Xb = reinterpret_cast<const __nv_bfloat16*>(X);
+    const __nv_bfloat16* Eb = reinterpret_cast<const __nv_bfloat16*>(E);
+
+    ce_lse_kernel<<<ceil_div(T, 8), 256, 0, s>>>(Xb, Eb, target, loss, lse, T, h, v_valid, d_status);
+    if (cudaGetLastError() != cudaSuccess) return MP_ERR_CUDA;
+
+    const int vs = v_pad / t;
+    const double Tb = 2.0 * T, hb = 2.0 * h, vb = 2.0 * vs;
+    const unsigned long long budget = wait_budget_ns();
+    for (int i = 0; i < t; ++i) {
+        const __nv_bfloat16* Ei = Eb + static_cast<long long>(i) * vs * h;
+        __nv_bfloat16* dEi = reinterpret_cast<__nv_bfloat16*>(dE) + static_cast<long long>(i) * vs * h;
+
+        // K10: z_i = X E_i^T -> dZ_i (bf16, [T, vs]) in the workspace.
+        TmapSet m10{};
+        if (!make_tmap_bf16(&m10.a, X, h, T, h, 64, BM) || !make_tmap_bf16(&m10.b, Ei, h, vs, h, 64, 128) ||
+            !make_tmap_bf16_out(&m10.o0, dz, vs, T, vs))
+            return MP_ERR_CUDA;
+        GemmArgs a10{};
+        a10.pr.M = T;
+        a10.pr.N = vs;
+        a10.pr.num_m_blocks = ceil_div(T, 2 * BM);
+        a10.pr.num_units = a10.pr.num_m_blocks * ceil_div(vs, 256);
+        a10.pr.n_fastest = n_fastest_order(Tb * h, vb * h);
+        a10.pr.kb_begin = 0;
+        a10.pr.kb_end = h / BK;
+        a10.tiles_per_unit = 1;
+        a10.target = target;
+        a10.v_valid = v_valid;
+        a10.col_off = i * vs;
+        a10.lse = lse;
+        a10.dloss = dloss;
+        a10.status = d_status;
+        a10.budget_ns = budget;
+        if (launch_gemm_tc<256, EPI_DZ, 8>(m10, a10, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+
+        // K11: dE_i = dZ_i^T X (M = vs, N = h, K = T; both operands MN-major).
+        TmapSet m11{};
+        if (!make_tmap_bf16(&m11.a, dz, vs, T, vs, 64, 64) || !make_tmap_bf16(&m11.b, X, h, T, h, 64, 64) ||
+            !make_tmap_bf16_out(&m11.o0, dEi, h, vs, h))
+            return MP_ERR_CUDA;
+        GemmArgs a11{};
+        a11.pr.M = vs;
+        a11.pr.N = h;
+        a11.pr.num_m_blocks = ceil_div(vs, 2 * BM);
+        a11.pr.num_units = a11.pr.num_m_blocks * ceil_div(h, 256);
+        a11.pr.n_fastest = n_fastest_order(Tb * vs, Tb * h);
+        a11.pr.kb_begin = 0;
+        a11.pr.kb_end = ceil_div(T, BK);
+        a11.pr.a_mn = 1;
+        a11.pr.b_mn = 1;
+        a11.tiles_per_unit = 1;
+        a11.status = d_status;
+        a11.budget_ns = budget;
+        if (launch_gemm_tc<256, EPI_STORE, 4>(m11, a11, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+
+        // K12: dX (+)= dZ_i E_i (M = T, N = h, K = vs; A K-major, B = E_i MN-major), shards in order.
+        TmapSet m12{};
+        if (!make_tmap_bf16(&m12.a, dz, vs, T, vs, 64, BM) || !make_tmap_bf16(&m12.b, Ei, h, vs, h, 64, 64) ||
+            !make_tmap_bf16_out(&m12.o0, dX, h, T, h))
+            return MP_ERR_CUDA;
+        GemmArgs a12{};
+        a12.pr.M = T;
+        a12.pr.N = h;
+        a12.pr.num_m_blocks = ceil_div(T, 2 * BM);
+        a12.pr.num_units = a12.pr.num_m_blocks * ceil_div(h, 256);
+        a12.pr.n_fastest = n_fastest_order(Tb * vs, vb * h);
+        a12.pr.kb_begin = 0;
+        a12.pr.kb_end = vs / BK;
+        a12.pr.a_mn = 0;
+        a12.pr.b_mn = 1;
+        a12.tiles_per_unit = 1;
+        a12.acc = acc;
+        a12.ld_acc = h;
+        a12.acc_mode = (t == 1) ? ACC_ONLY : (i == 0 ? ACC_FIRST : (i == t - 1 ? ACC_LAST : ACC_MID));
+        a12.status = d_status;
+        a12.budget_ns = budget;
+        if (launch_gemm_tc<256, EPI_ACC, 4>(m12, a12, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+    }
+    return MP_OK;
+}

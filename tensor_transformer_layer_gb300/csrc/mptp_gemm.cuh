@@ -62,6 +62,15 @@ enum EpiKind : int {
     EPI_GELU = 1,   // out0 = bf16(GeLU(acc)); out1 (nullable) = bf16(acc)
     EPI_DGELU = 2,  // out0 = bf16(acc * GeLU'(aux)), aux = bf16 U
     EPI_CE = 3,     // per-row online max / sum-exp / target logit over the unit
+    EPI_DZ = 4,     // out0 = bf16(dloss * (exp(acc - lse) - [col == target])), 0 on padding columns
+    EPI_ACC = 5,    // fp32 accumulation across launches into `acc`; the last launch stores bf16 out0
+};
+
+enum AccMode : int {
+    ACC_FIRST = 0,  // acc = C
+    ACC_MID = 1,    // acc += C
+    ACC_LAST = 2,   // out0 = bf16(acc + C)
+    ACC_ONLY = 3,   // out0 = bf16(C)
 };
 
 // The GEMM of a launch.
@@ -81,10 +90,17 @@ struct GemmArgs {
     const __nv_bfloat16* aux; // U for GeLU'
     long long ld_aux;
     int has_out1;             // GeLU: also store U (tensor map o1)
-    // cross-entropy epilogue
+    // cross-entropy epilogues
     const int32_t* target;
     float* ws;                // [P][3][M] fp32: max, sum-exp, target logit
     int v_valid;
+    int col_off;              // global vocabulary index of output column 0 (backward: shard offset)
+    const float* lse;         // backward: per-token log-sum-exp (NaN = invalid target)
+    const float* dloss;       // backward: per-token upstream gradient
+    // fp32 accumulation across launches
+    float* acc;
+    long long ld_acc;
+    int acc_mode;
     uint32_t* status;         // nullable
     unsigned long long budget_ns;
 };
@@ -120,6 +136,7 @@ struct GemmCfg {
     static_assert(BN == 128 || BN == 256, "pair tile width");
     static_assert(NE == 4 || NE == 8, "4 or 8 epilogue warps");
     static_assert(EPI != EPI_CE || NE == 4, "cross-entropy epilogue keeps one thread per row");
+    static_assert(EPI != EPI_ACC || NE == 4, "accumulating epilogue uses four warps");
 };
 
 struct Ctl {
@@ -425,7 +442,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
             // cross-entropy running state (natural-log units)
             float run_m = -INFINITY, run_s = 0.0f, z_tgt = 0.0f;
             int tgt = -1;
-            if (EPI == EPI_CE && row_ok) tgt = args.target[row];
+            if ((EPI == EPI_CE || EPI == EPI_DZ) && row_ok) tgt = args.target[row];
+            // cross-entropy backward row state: lse in log2 units, upstream gradient
+            float lse2 = 0.0f, dl = 0.0f;
+            if (EPI == EPI_DZ && row_ok) {
+                lse2 = args.lse[row] * 1.4426950408889634f;
+                dl = args.dloss[row];
+                if (!(lse2 == lse2)) {  // invalid target (NaN log-sum-exp): no gradient for this token
+                    lse2 = 0.0f;
+                    dl = 0.0f;
+                    tgt = -1;
+                }
+            }
 
             for (int nt = 0; nt < args.tiles_per_unit; ++nt, ++tcount) {
                 const uint32_t buf = tcount & 1u;
@@ -493,6 +521,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                             pk[j] = pack_bf16x2(g0, g1);
                         }
                         stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
+                    } else if constexpr (EPI == EPI_DZ) {
+                        // dZ = dloss * (softmax - onehot) on valid columns, 0 on padding.
+                        constexpr float LOG2E = 1.4426950408889634f;
+                        const int gcol0 = args.col_off + col0;
+                        const int lim = args.v_valid - gcol0;
+                        const unsigned dt = static_cast<unsigned>(tgt - gcol0);
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            float g[2];
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const int jj = 2 * j + e2;
+                                float pr = ex2_approx(fmaf(__uint_as_float(r[jj]), LOG2E, -lse2));
+                                if (static_cast<int>(dt) == jj && dt < 32u) pr -= 1.0f;
+                                g[e2] = (jj < lim && dl != 0.0f) ? dl * pr : 0.0f;
+                            }
+                            pk[j] = pack_bf16x2(g[0], g[1]);
+                        }
+                        stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
+                    } else if constexpr (EPI == EPI_ACC) {
+                        if (args.acc_mode == ACC_ONLY || args.acc_mode == ACC_LAST) {
+                            float v[32];
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                            if (args.acc_mode == ACC_LAST && row_ok) {
+                                const float4* src = reinterpret_cast<const float4*>(args.acc + row * args.ld_acc + col0);
+#pragma unroll
+                                for (int j = 0; j < 8; ++j) {
+                                    const float4 a4 = src[j];
+                                    v[4 * j] += a4.x;
+                                    v[4 * j + 1] += a4.y;
+                                    v[4 * j + 2] += a4.z;
+                                    v[4 * j + 3] += a4.w;
+                                }
+                            }
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+                            stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
+                        } else if (row_ok) {
+                            float4* dst = reinterpret_cast<float4*>(args.acc + row * args.ld_acc + col0);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                float4 c4 = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                                if (args.acc_mode == ACC_MID) {
+                                    const float4 a4 = dst[j];
+                                    c4.x += a4.x;
+                                    c4.y += a4.y;
+                                    c4.z += a4.z;
+                                    c4.w += a4.w;
+                                }
+                                dst[j] = c4;
+                            }
+                        }
                     } else {  // EPI_CE
                         const int lim = args.v_valid - col0;  // valid columns in this chunk
                         if (lim > 0) {
