@@ -316,12 +316,32 @@ def time_next_rows(step, reps, flush):
     ts.sort()
     ms = ts[len(ts) // 2]
     step.check_status()
+    # vocab-parallel input embedding of the same T tokens (ids = the targets)
+    emb = torch.empty(T, h, dtype=torch.bfloat16, device=d["Xc"].device)
+    efn = lambda: mp.mp_vocab_embed(d["target"], d["E"], emb, v_valid=v_valid, t=t, d_status=step.status)
+    efn()
+    ets = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        efn()
+        b.record()
+        torch.cuda.synchronize()
+        ets.append(a.elapsed_time(b))
+    ets.sort()
+    ems = ets[len(ets) // 2]
+    ebytes = 2.0 * T * h * 2 + 4.0 * T   # read T rows of E, write T rows, read the ids
+    peaks, peak_src = load_peaks()
+    embed = {"ms": ems, "gbs": ebytes / (ems * 1e-3) / 1e9, "bytes": ebytes,
+             "frac_of_hbm": ebytes / (ems * 1e-3) / 1e9 / peaks["hbm_gbs"], "hbm_peak_source": peak_src}
     algo = 4.0 * T * h * v_pad      # dX = dZ E and dE = dZ^T X
     executed = 6.0 * T * h * v_pad  # plus the logit recompute (logits are never stored)
     return {"ce_bwd": {"ms": ms, "tflops_algorithmic": algo / (ms * 1e-3) / 1e12,
                        "tflops_executed": executed / (ms * 1e-3) / 1e12, "tokens_per_s": T / (ms * 1e-3),
                        "launches": 1 + 3 * t,
-                       "flop_note": "algorithmic 4*T*h*v_pad (dX, dE); executed adds the 2*T*h*v_pad recompute"}}
+                       "flop_note": "algorithmic 4*T*h*v_pad (dX, dE); executed adds the 2*T*h*v_pad recompute"},
+            "vocab_embed": embed}
 
 
 def time_e2e(step, steps, warmup):

@@ -183,6 +183,21 @@ MP_API mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const int32
                           uint32_t* d_status, void* stream);
 
 /*
+ * Vocab-parallel input embedding ("Megatron-LM: Training Multi-Billion Parameter
+ * Language Models Using Model Parallelism", section 3.4 "Input Embedding
+ * Parallelism"): E [v_pad, h] split along the vocabulary into t shards of v_pad/t
+ * rows; each shard looks up the ids in its range (zeros elsewhere) and the shards'
+ * results are summed (the g all-reduce). One shard owns each valid id, so
+ *   out[r] = E[ids[r]] exactly (bit for bit) for ids in [0, v_valid);
+ *   out[r] = 0 and MP_DEV_TARGET_RANGE set for any other id (no shard owns it).
+ *   ids [T] int32, E [v_pad, h] bf16, out [T, h] bf16 (overwritten).
+ *   Size rules: h % 64 == 0; t >= 1; v_pad % (128 t) == 0; 1 <= v_valid <= v_pad.
+ */
+MP_API mp_status mp_vocab_embed(const int32_t* ids, const mp_bf16* E, mp_bf16* out,
+                         int T, int h, int v_pad, int v_valid, int t,
+                         uint32_t* d_status, void* stream);
+
+/*
  * mp_vocab_ce for callers that cannot allocate device memory. The paper has no
  * counterpart to this entry point; it exists for callers whose device memory is
  * owned by another pool (a serving runtime that reserves HBM at start-up and

@@ -12,7 +12,8 @@ definition states. Sources, cited by page title and section:
 [p1] "Megatron-LM: Training Multi-Billion Parameter Language Models Using Model
      Parallelism" (paper-graph-ui summary), §3.4 "Detailed, Sentence-Based
      Technical Breakdown": column-parallel GEMM, row-parallel GEMM, g/f
-     operators, fused vocab-parallel cross-entropy, vocabulary padding.
+     operators, vocab-parallel input embedding, fused vocab-parallel
+     cross-entropy, vocabulary padding.
 [p3] "Tensor and pipeline parallelism, and choosing a layout" (ML Systems,
      lesson 9), §3 "Definitions and main results", Proposition (Megatron MLP
      split), proof steps 1-5 (forward and backward).
@@ -43,6 +44,7 @@ from .mlp import (
 from .ce import (ce_loss, ce_partition_triples, ce_combine, ce_loss_partitioned, ce_bwd, ce_logsumexp,
                  ce_bwd_sampled)
 from .padding import pad_vocab
+from .embed import embed_sharded
 
 __all__ = [
     "gelu", "gelu_prime", "std_normal_cdf", "std_normal_pdf",
@@ -50,5 +52,5 @@ __all__ = [
     "mlp_fwd_rows", "mlp_bwd_sampled",
     "ce_loss", "ce_partition_triples", "ce_combine", "ce_loss_partitioned", "ce_bwd", "ce_logsumexp",
     "ce_bwd_sampled",
-    "pad_vocab",
+    "pad_vocab", "embed_sharded",
 ]

@@ -32,7 +32,7 @@ STATUS_NAMES = {
 # Every symbol include/mptp.h declares.
 EXPORTS = ("mp_mlp_fwd", "mp_mlp_bwd", "mp_vocab_ce_workspace_bytes", "mp_vocab_ce", "mp_vocab_ce_partials",
            "mp_vocab_ce_combine", "mp_status_string", "mp_status_from_device", "mp_version",
-           "mp_vocab_ce_noalloc", "mp_vocab_ce_bwd_workspace_bytes", "mp_vocab_ce_bwd")
+           "mp_vocab_ce_noalloc", "mp_vocab_ce_bwd_workspace_bytes", "mp_vocab_ce_bwd", "mp_vocab_embed")
 
 
 class MptpError(RuntimeError):
@@ -70,6 +70,8 @@ def lib() -> ctypes.CDLL:
         L.mp_vocab_ce_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.mp_vocab_ce_bwd.argtypes = [_P] * 7 + [_P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P, _P]
         L.mp_vocab_ce_bwd.restype = _I
+        L.mp_vocab_embed.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]
+        L.mp_vocab_embed.restype = _I
         L.mp_vocab_ce_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]
         L.mp_vocab_ce_noalloc.restype = _I
         L.mp_status_string.argtypes = [_I]
@@ -224,6 +226,16 @@ def mp_vocab_ce_bwd(X, E, target, loss, dloss, dX, dE, workspace, *, v_valid: in
         _ptr(dE, "dE", shape=(v_pad, h)), wp, wb, T, h, v_pad, int(v_valid), int(t), _status_ptr(d_status),
         _stream(stream))
     _check("mp_vocab_ce_bwd", code)
+
+
+def mp_vocab_embed(ids, E, out, *, v_valid: int, t: int, d_status=None, stream=None) -> None:
+    """Vocab-parallel embedding lookup: out[r] = E[ids[r]] (zeros for ids outside [0, v_valid))."""
+    T = ids.shape[0]
+    v_pad, h = E.shape
+    code = lib().mp_vocab_embed(
+        _ptr(ids, "ids", dtype=torch.int32, shape=(T,)), _ptr(E, "E", shape=(v_pad, h)),
+        _ptr(out, "out", shape=(T, h)), T, h, v_pad, int(v_valid), int(t), _status_ptr(d_status), _stream(stream))
+    _check("mp_vocab_embed", code)
 
 
 def mp_status_from_device(bits: int) -> int:
