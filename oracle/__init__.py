@@ -18,7 +18,8 @@ definition states. Sources, cited by page title and section:
      lesson 9), §3 "Definitions and main results", Proposition (Megatron MLP
      split), proof steps 1-5 (forward and backward).
 [p5] "Megatron-LM, annotated" (ai-primer), §2.2 (GELU, erf form), §3.1 (the
-     two-token MLP example), §3.4 (embedding, loss, vocabulary padding).
+     two-token MLP example), §3.2 (attention block), §3.4 (embedding, loss,
+     vocabulary padding).
 
 The cross-entropy backward (``ce_bwd``) is not spelled out on the pages, which
 train the model but describe only the forward fusion; it is the plain derivative
@@ -45,6 +46,7 @@ from .ce import (ce_loss, ce_partition_triples, ce_combine, ce_loss_partitioned,
                  ce_bwd_sampled)
 from .padding import pad_vocab
 from .embed import embed_sharded
+from .attn import attention_heads, attn_fwd, attn_fwd_sharded, attn_fwd_rows
 
 __all__ = [
     "gelu", "gelu_prime", "std_normal_cdf", "std_normal_pdf",
@@ -53,4 +55,5 @@ __all__ = [
     "ce_loss", "ce_partition_triples", "ce_combine", "ce_loss_partitioned", "ce_bwd", "ce_logsumexp",
     "ce_bwd_sampled",
     "pad_vocab", "embed_sharded",
+    "attention_heads", "attn_fwd", "attn_fwd_sharded", "attn_fwd_rows",
 ]
