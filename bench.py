@@ -335,13 +335,44 @@ def time_next_rows(step, reps, flush):
     peaks, peak_src = load_peaks()
     embed = {"ms": ems, "gbs": ebytes / (ems * 1e-3) / 1e9, "bytes": ebytes,
              "frac_of_hbm": ebytes / (ems * 1e-3) / 1e9 / peaks["hbm_gbs"], "hbm_peak_source": peak_src}
+    # head-parallel causal attention block at the 8.3B-layer shape (b = 4, s = 1024, 32 heads of 96, t = 8)
+    import synth
+    ab, as_, ah, aheads, at = 4, 1024, MLP["h"], 32, MLP["t"]
+    aT = ab * as_
+    ax = synth.normal_bf16((aT, ah), 1.0, 1005).to(d["Xc"].device)
+    awqkv = synth.normal_bf16((ah, 3 * ah), 0.02, 1006).to(d["Xc"].device)
+    awo = synth.normal_bf16((ah, ah), 0.02, 1007).to(d["Xc"].device)
+    aout = torch.empty(aT, ah, dtype=torch.bfloat16, device=d["Xc"].device)
+    aqkv = torch.empty(aT, 3 * ah, dtype=torch.bfloat16, device=d["Xc"].device)
+    ao = torch.empty(aT, ah, dtype=torch.bfloat16, device=d["Xc"].device)
+    afn = lambda: mp.mp_attn_fwd(ax, awqkv, awo, aout, aqkv, ao, b=ab, s=as_, heads=aheads, t=at,
+                                 d_status=step.status)
+    afn()
+    ats = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        afn()
+        b_.record()
+        torch.cuda.synchronize()
+        ats.append(a.elapsed_time(b_))
+    ats.sort()
+    ams = ats[len(ats) // 2]
+    hd = ah // aheads
+    attn_core = 4.0 * ab * aheads * hd * as_ * (as_ + 1) / 2     # QK^T and PV over the causal pairs
+    attn_flop = 2.0 * aT * ah * 3 * ah + attn_core + 2.0 * aT * ah * ah
+    attn = {"ms": ams, "tflops": attn_flop / (ams * 1e-3) / 1e12, "flop": attn_flop,
+            "shape": {"b": ab, "s": as_, "h": ah, "heads": aheads, "head_dim": hd, "t": at},
+            "flop_note": "QKV 6*T*h^2 + causal attention 4*b*heads*d*s(s+1)/2 + out 2*T*h^2; launches 3"}
     algo = 4.0 * T * h * v_pad      # dX = dZ E and dE = dZ^T X
     executed = 6.0 * T * h * v_pad  # plus the logit recompute (logits are never stored)
     return {"ce_bwd": {"ms": ms, "tflops_algorithmic": algo / (ms * 1e-3) / 1e12,
                        "tflops_executed": executed / (ms * 1e-3) / 1e12, "tokens_per_s": T / (ms * 1e-3),
                        "launches": 1 + 3 * t,
                        "flop_note": "algorithmic 4*T*h*v_pad (dX, dE); executed adds the 2*T*h*v_pad recompute"},
-            "vocab_embed": embed}
+            "vocab_embed": embed,
+            "attn_fwd": attn}
 
 
 def time_e2e(step, steps, warmup):

@@ -198,6 +198,25 @@ MP_API mp_status mp_vocab_embed(const int32_t* ids, const mp_bf16* E, mp_bf16* o
                          uint32_t* d_status, void* stream);
 
 /*
+ * Forward of the head-parallel self-attention block ("Megatron-LM: Training
+ * Multi-Billion Parameter Language Models Using Model Parallelism", section 3.4
+ * "Attention Head Parallelism in the Self-Attention Block"; "Megatron-LM,
+ * annotated", section 3.2): heads are split across t shards by the columns of the
+ * Q, K, V projections; each head runs causal softmax attention (GPT-2 decoder);
+ * the output projection is split by rows and the shards' partials are summed (g).
+ *   QKV = X Wqkv;  O[:, head j] = softmax(Q_j K_j^T / sqrt(d) + causal) V_j;
+ *   out = sum_i O_i Wo_i (shards in ascending order inside the GEMM K-loop).
+ *   X [b s, h] (b sequences of s tokens), Wqkv [h, 3h] = [Wq | Wk | Wv] with head j at
+ *   columns [j d, (j+1) d) of each, Wo [h, h]; outputs QKV [b s, 3h], O [b s, h] (both
+ *   kept for a backward pass) and out [b s, h], bf16, overwritten.
+ *   Size rules: d = h / heads in {64, 96}; heads % t == 0; h % 64 == 0; s % 128 == 0.
+ */
+MP_API mp_status mp_attn_fwd(const mp_bf16* X, const mp_bf16* Wqkv, const mp_bf16* Wo,
+                      mp_bf16* out, mp_bf16* QKV, mp_bf16* O,
+                      int b, int s, int h, int heads, int t,
+                      uint32_t* d_status, void* stream);
+
+/*
  * mp_vocab_ce for callers that cannot allocate device memory. The paper has no
  * counterpart to this entry point; it exists for callers whose device memory is
  * owned by another pool (a serving runtime that reserves HBM at start-up and

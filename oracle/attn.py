@@ -75,21 +75,24 @@ def attn_fwd_sharded(X, Wqkv, Wo, heads: int, b: int, s: int, t: int):
 
 
 def attn_fwd_rows(X, Wqkv, Wo, heads: int, b: int, s: int, rows):
-    """out[rows] and O[rows]: a query row needs its sequence's keys and values up to itself."""
+    """out[rows] and O[rows]: a query row needs its own sequence's keys and values up
+    to itself, so each sampled sequence's projections are formed once (up to its last
+    sampled row) and the rows' attention is taken from them."""
     X, Wqkv, Wo = _f64(X), _f64(Wqkv), _f64(Wo)
     h = X.shape[1]
     d = h // heads
     rows = np.asarray(rows)
     O = np.zeros((len(rows), h))
-    for n, r in enumerate(rows):
-        q0 = (r // s) * s
-        Xs = X[q0:r + 1]
-        Qr = X[r] @ Wqkv[:, :h]
-        Ks = Xs @ Wqkv[:, h:2 * h]
-        Vs = Xs @ Wqkv[:, 2 * h:]
-        for j in range(heads):
-            c = slice(j * d, (j + 1) * d)
-            sc = Ks[:, c] @ Qr[c] / np.sqrt(d)
-            p = np.exp(sc - sc.max())
-            O[n, c] = (p / p.sum()) @ Vs[:, c]
+    for q in np.unique(rows // s):
+        sel = np.nonzero(rows // s == q)[0]
+        last = int(rows[sel].max())
+        q0 = q * s
+        QKV = X[q0:last + 1] @ Wqkv
+        for n in sel:
+            i = int(rows[n]) - q0
+            for j in range(heads):
+                c = slice(j * d, (j + 1) * d)
+                sc = QKV[:i + 1, h + j * d:h + (j + 1) * d] @ QKV[i, c] / np.sqrt(d)
+                p = np.exp(sc - sc.max())
+                O[n, c] = (p / p.sum()) @ QKV[:i + 1, 2 * h + j * d:2 * h + (j + 1) * d]
     return O, O @ Wo

@@ -32,7 +32,8 @@ STATUS_NAMES = {
 # Every symbol include/mptp.h declares.
 EXPORTS = ("mp_mlp_fwd", "mp_mlp_bwd", "mp_vocab_ce_workspace_bytes", "mp_vocab_ce", "mp_vocab_ce_partials",
            "mp_vocab_ce_combine", "mp_status_string", "mp_status_from_device", "mp_version",
-           "mp_vocab_ce_noalloc", "mp_vocab_ce_bwd_workspace_bytes", "mp_vocab_ce_bwd", "mp_vocab_embed")
+           "mp_vocab_ce_noalloc", "mp_vocab_ce_bwd_workspace_bytes", "mp_vocab_ce_bwd", "mp_vocab_embed",
+           "mp_attn_fwd")
 
 
 class MptpError(RuntimeError):
@@ -70,6 +71,8 @@ def lib() -> ctypes.CDLL:
         L.mp_vocab_ce_bwd_workspace_bytes.restype = ctypes.c_size_t
         L.mp_vocab_ce_bwd.argtypes = [_P] * 7 + [_P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P, _P]
         L.mp_vocab_ce_bwd.restype = _I
+        L.mp_attn_fwd.argtypes = [_P] * 6 + [_I, _I, _I, _I, _I, _P, _P]
+        L.mp_attn_fwd.restype = _I
         L.mp_vocab_embed.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]
         L.mp_vocab_embed.restype = _I
         L.mp_vocab_ce_noalloc.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P]
@@ -236,6 +239,19 @@ def mp_vocab_embed(ids, E, out, *, v_valid: int, t: int, d_status=None, stream=N
         _ptr(ids, "ids", dtype=torch.int32, shape=(T,)), _ptr(E, "E", shape=(v_pad, h)),
         _ptr(out, "out", shape=(T, h)), T, h, v_pad, int(v_valid), int(t), _status_ptr(d_status), _stream(stream))
     _check("mp_vocab_embed", code)
+
+
+def mp_attn_fwd(X, Wqkv, Wo, out, QKV, O, *, b: int, s: int, heads: int, t: int, d_status=None,
+                stream=None) -> None:
+    """Head-parallel causal self-attention block: QKV = X Wqkv, per-head attention O, out = O Wo."""
+    T, h = X.shape
+    if T != b * s:
+        raise ValueError("X must have b * s rows")
+    code = lib().mp_attn_fwd(
+        _ptr(X, "X", shape=(T, h)), _ptr(Wqkv, "Wqkv", shape=(h, 3 * h)), _ptr(Wo, "Wo", shape=(h, h)),
+        _ptr(out, "out", shape=(T, h)), _ptr(QKV, "QKV", shape=(T, 3 * h)), _ptr(O, "O", shape=(T, h)),
+        int(b), int(s), h, int(heads), int(t), _status_ptr(d_status), _stream(stream))
+    _check("mp_attn_fwd", code)
 
 
 def mp_status_from_device(bits: int) -> int:

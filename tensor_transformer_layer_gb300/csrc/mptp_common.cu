@@ -43,6 +43,11 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t
     return make_tmap_bf16_sw(map, base, inner, outer, pitch_elems, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+bool make_tmap_bf16_sw64(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
+                         uint32_t box_inner, uint32_t box_outer) {
+    return make_tmap_bf16_sw(map, base, inner, outer, pitch_elems, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
 bool make_tmap_bf16_out(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems) {
     return make_tmap_bf16_sw(map, base, inner, outer, pitch_elems, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }

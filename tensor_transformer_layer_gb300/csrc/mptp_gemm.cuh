@@ -106,7 +106,7 @@ struct GemmArgs {
 };
 
 // Tensor maps of a launch: the two operands and the epilogue outputs.
-struct alignas(64) TmapSet {
+struct TmapSet {
     CUtensorMap a;
     CUtensorMap b;
     CUtensorMap o0;

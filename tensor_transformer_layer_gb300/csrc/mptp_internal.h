@@ -17,6 +17,10 @@ namespace mptp {
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
                     uint32_t box_inner, uint32_t box_outer);
 
+// Same with the 64-byte swizzle (boxes up to 32 bf16 wide).
+bool make_tmap_bf16_sw64(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
+                         uint32_t box_inner, uint32_t box_outer);
+
 // Tensor map for an epilogue output: 32 x 32 boxes, 64-byte swizzle (the layout
 // the epilogue stages rows in before its TMA store).
 bool make_tmap_bf16_out(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems);

@@ -266,6 +266,20 @@ __device__ __forceinline__ uint64_t make_sdesc_sw128(uint32_t saddr, uint32_t lb
     return d;
 }
 
+// Same descriptor with the 64-byte swizzle (swizzle atom 8 rows x 64 bytes):
+// K-major rows are 64 B apart (SBO = 512 between 8-row groups, a 16-wide K slice is
+// 32 B); MN-major atoms hold 32 M/N elements x 8 k rows (LBO between 32-wide blocks,
+// SBO = 512 between 8-row k groups).
+__device__ __forceinline__ uint64_t make_sdesc_sw64(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(4) << 61;
+    return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D:
 //   [4,6) D format (1 = f32)  [7,10) A format (1 = bf16)  [10,13) B format (1 = bf16)
 //   [15] A major (0 = K, 1 = MN)  [16] B major  [17,23) N >> 3  [24,29) M >> 4
