@@ -527,7 +527,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
     ap.add_argument("--sweep", action="store_true",
                     help="time MLP fwd+bwd and the fused CE at every point of the layer sweep (one JSON line each)")
-    ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "mlp"), default="none",
+    ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "mlp", "attn"), default="none",
                     help="run only a small case of one entry point a few times (for ncu), print nothing")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.profile_case == "none":
@@ -692,6 +692,17 @@ def profile_case(which, dev):
 
     import synth
     import tensor_transformer_layer_gb300 as mp
+    if which == "attn":
+        b, s_, h, heads, t = 4, 1024, MLP["h"], 32, MLP["t"]
+        X = synth.normal_bf16((b * s_, h), 1.0, 1005).to(dev)
+        Wqkv = synth.normal_bf16((h, 3 * h), 0.02, 1006).to(dev)
+        Wo = synth.normal_bf16((h, h), 0.02, 1007).to(dev)
+        e = lambda *sh: torch.empty(*sh, dtype=torch.bfloat16, device=dev)
+        out, QKV, O = e(b * s_, h), e(b * s_, 3 * h), e(b * s_, h)
+        for _ in range(3):
+            mp.mp_attn_fwd(X, Wqkv, Wo, out, QKV, O, b=b, s=s_, heads=heads, t=t)
+        torch.cuda.synchronize()
+        return 0
     if which in ("ce", "ce_full"):
         T, h, v_pad, v_valid, t = (2048 if which == "ce" else CE["T"]), 1536, 51200, 50257, 8
         ci = synth.ce_inputs(T, h, v_pad, v_valid, seed=1002)
