@@ -525,6 +525,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("mptp", "reference"), default="mptp")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
+    ap.add_argument("--no-next-rows", action="store_true", help="skip the rows measured beside the step")
     ap.add_argument("--sweep", action="store_true",
                     help="time MLP fwd+bwd and the fused CE at every point of the layer sweep (one JSON line each)")
     ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "mlp", "attn"), default="none",
@@ -575,7 +576,7 @@ def main(argv=None):
     value = world * step_flop() * args.steps / (total_ms * 1e-3) / 1e12
 
     breakdown = time_breakdown(step, 9, flush)
-    next_rows = time_next_rows(step, 9, flush)
+    next_rows = None if args.no_next_rows else time_next_rows(step, 9, flush)
     peaks, peak_src = load_peaks()
     ce_avg_ms = sum(ce_ms) / len(ce_ms)
     ce_achieved = ce_flop() / (ce_avg_ms * 1e-3) / 1e12
