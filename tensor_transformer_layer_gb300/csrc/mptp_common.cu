@@ -110,6 +110,80 @@ bool ce_plan(int v_pad, int t, CePlan* plan) {
     return true;
 }
 
+namespace {
+struct SideEntry {
+    bool tried;
+    bool ok;
+    SideStreams ss;
+};
+std::mutex g_side_mu;
+SideEntry g_side[64];
+}  // namespace
+
+std::mutex& side_stream_mutex() { return g_side_mu; }
+
+SideStreams* side_streams(cudaStream_t origin) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    SideEntry& e = g_side[dev];
+    if (!e.tried) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(origin, &cs) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        if (cs != cudaStreamCaptureStatusNone) return nullptr;
+        e.tried = true;
+        bool ok = true;
+        for (int i = 0; i < 2; ++i)
+            ok = ok && cudaStreamCreateWithFlags(&e.ss.s[i], cudaStreamNonBlocking) == cudaSuccess;
+        ok = ok && cudaEventCreateWithFlags(&e.ss.fork, cudaEventDisableTiming) == cudaSuccess;
+        for (int i = 0; i < 2; ++i)
+            ok = ok && cudaEventCreateWithFlags(&e.ss.join[i], cudaEventDisableTiming) == cudaSuccess;
+        if (!ok) cudaGetLastError();
+        e.ok = ok;
+    }
+    return e.ok ? &e.ss : nullptr;
+}
+
+static long long rounds_cost(int units, int c, int cost) {
+    return static_cast<long long>((units + c - 1) / c) * cost;
+}
+
+long long split_pairs(int pairs, int n, const int* units, const int* cost, int* split) {
+    long long best = -1;
+    int c[3] = {1, 1, 1};
+    const int c0_max = pairs - (n - 1);
+    for (c[0] = 1; c[0] <= c0_max; ++c[0]) {
+        const int c1_max = n > 1 ? pairs - c[0] - (n - 2) : 1;
+        for (c[1] = 1; c[1] <= c1_max; ++c[1]) {
+            if (n > 2) c[2] = pairs - c[0] - c[1];
+            long long span = 0;
+            int use[3];
+            for (int i = 0; i < n; ++i) {
+                use[i] = c[i] < units[i] ? c[i] : units[i];
+                const long long r = rounds_cost(units[i], use[i], cost[i]);
+                span = r > span ? r : span;
+            }
+            if (best < 0 || span < best) {
+                best = span;
+                for (int i = 0; i < n; ++i) split[i] = use[i];
+            }
+            if (n == 1) break;
+        }
+    }
+    return best;
+}
+
+long long serial_makespan(int pairs, int n, const int* units, const int* cost) {
+    long long t = 0;
+    for (int i = 0; i < n; ++i) t += rounds_cost(units[i], units[i] < pairs ? units[i] : pairs, cost[i]);
+    return t;
+}
+
 }  // namespace mptp
 
 extern "C" const char* mp_status_string(mp_status s) {

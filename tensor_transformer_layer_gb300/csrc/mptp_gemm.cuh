@@ -684,15 +684,17 @@ inline int resident_pairs(int num_sms) {
     return clusters;
 }
 
-// Host-side launcher: grid = 2 x min(units, resident pairs), one CTA per SM.
+// Host-side launcher: grid = 2 x min(units, resident pairs, max_pairs if > 0), one CTA per SM.
 template <int BN, int EPI, int NE>
-inline cudaError_t launch_gemm_tc(const TmapSet& maps, const GemmArgs& args, int num_sms, cudaStream_t stream) {
+inline cudaError_t launch_gemm_tc(const TmapSet& maps, const GemmArgs& args, int num_sms, cudaStream_t stream,
+                                  int max_pairs = 0) {
     using Cfg = GemmCfg<BN, EPI, NE>;
     auto kern = gemm_tc_kernel<BN, EPI, NE>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    const int pairs = resident_pairs<BN, EPI, NE>(num_sms);
+    int pairs = resident_pairs<BN, EPI, NE>(num_sms);
+    if (max_pairs > 0 && max_pairs < pairs) pairs = max_pairs;
     const int use = args.pr.num_units < pairs ? args.pr.num_units : pairs;
     if (use <= 0) return cudaSuccess;
     kern<<<2 * use, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(maps, args);

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "mptp.h"
 
 namespace mptp {
@@ -49,5 +51,29 @@ struct CePlan {
     int P;               // v_pad / chunk_cols partitions
 };
 bool ce_plan(int v_pad, int t, CePlan* plan);
+
+// Two extra streams of the current device with fork/join events, for GEMMs that run
+// side by side with the caller's stream; every launch on them is still ordered after
+// the work the caller enqueued before (fork) and before the work it enqueues after
+// (join). Created on first use outside a stream capture and kept for the process.
+struct SideStreams {
+    cudaStream_t s[2];
+    cudaEvent_t fork;
+    cudaEvent_t join[2];
+};
+// Hold side_stream_mutex() from side_streams() until the join has been enqueued.
+std::mutex& side_stream_mutex();
+// nullptr if they cannot be created now (no device, out of resources, or `origin` is
+// being captured and they do not exist yet).
+SideStreams* side_streams(cudaStream_t origin);
+
+// Static split of `pairs` CTA pairs among n <= 3 GEMMs launched side by side. GEMM i has
+// units[i] output tiles of cost[i] (K blocks plus the epilogue); on c pairs it takes
+// ceil(units / c) rounds. Fills split[] and returns the makespan in cost units; a split
+// never gives a GEMM more pairs than it has units.
+long long split_pairs(int pairs, int n, const int* units, const int* cost, int* split);
+
+// Makespan of the same GEMMs one after another, each on all `pairs`.
+long long serial_makespan(int pairs, int n, const int* units, const int* cost);
 
 }  // namespace mptp

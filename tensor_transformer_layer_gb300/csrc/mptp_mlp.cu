@@ -10,6 +10,15 @@
 //   K3  dU = (G B^T) * GeLU'(U)
 //   K4  dX = sum_i dU_i A_i^T      K-loop over shards 0..t-1 (the f sum)
 //   K5  dA = X^T dU, dB = Y^T G    both operands MN-major, K = T
+// K4 and K5 are independent once dU exists. Megatron overlaps the backward all-reduce
+// of dX with the weight-gradient GEMMs ("Tensor and pipeline parallelism, and choosing
+// a layout", the discussion after the Proposition on the communication ratio); here
+// the f sum of dX is inside K4's K-loop, and the overlap becomes K4, K5a and K5b side
+// by side on disjoint sets of CTA pairs (the caller's stream plus two side streams),
+// so that none of them ends in a part-empty last wave of tiles.
+#include <cstdlib>
+#include <cstring>
+
 #include "mptp_gemm.cuh"
 #include "mptp_internal.h"
 
@@ -37,6 +46,22 @@ static ProbInfo problem(int M, int N, int bn, int kb_begin, int kb_end, bool a_m
     p.b_mn = b_mn ? 1 : 0;
     return p;
 }
+
+// Backward schedule of K4, K5a, K5b: MPTP_BWD_SCHEDULE = "serial" | "overlap"; unset or
+// anything else picks the side-by-side schedule when its estimated makespan is at least
+// 6 % below the serial one. Measured on GB300 over h in {768..3072}, T in {512..8192}:
+// it wins 1-50 % where the estimate says >= 7 %, and loses up to 5 % at h = 3072 with
+// T >= 4096 (estimate <= 5.5 %), where three GEMMs' operand panels crowd L2.
+enum class BwdSchedule { Auto, Serial, Overlap };
+static BwdSchedule bwd_schedule() {
+    const char* v = std::getenv("MPTP_BWD_SCHEDULE");
+    if (v != nullptr && std::strcmp(v, "serial") == 0) return BwdSchedule::Serial;
+    if (v != nullptr && std::strcmp(v, "overlap") == 0) return BwdSchedule::Overlap;
+    return BwdSchedule::Auto;
+}
+
+// Cost of one output tile in K-block times: its K blocks plus about two for the epilogue.
+constexpr int EPI_KB = 2;
 
 static GemmArgs launch_args(uint32_t* status) {
     GemmArgs a{};
@@ -131,7 +156,6 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
         return MP_ERR_CUDA;
     GemmArgs a4 = launch_args(d_status);
     a4.pr = problem(T, h, 256, 0 * (fs / BK), t * (fs / BK), false, false, Tb * f, hb * f);
-    if (launch_gemm_tc<256, EPI_STORE, 4>(m4, a4, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
     // K5a: dA = X^T dU (M = h, N = f, K = T).  Both operands MN-major.
     TmapSet m5{};
@@ -140,7 +164,6 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
         return MP_ERR_CUDA;
     GemmArgs a5 = launch_args(d_status);
     a5.pr = problem(h, f, 256, 0, ceil_div(T, BK), true, true, Tb * h, Tb * f);
-    if (launch_gemm_tc<256, EPI_STORE, 4>(m5, a5, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
     // K5b: dB = Y^T dZ (M = f, N = h, K = T).  Both operands MN-major.
     TmapSet m6{};
@@ -149,6 +172,41 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
         return MP_ERR_CUDA;
     GemmArgs a6 = launch_args(d_status);
     a6.pr = problem(f, h, 256, 0, ceil_div(T, BK), true, true, Tb * f, Tb * h);
-    if (launch_gemm_tc<256, EPI_STORE, 4>(m6, a6, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+
+    // Every output tile is computed by the same K-loop whichever pairs run it, so both
+    // schedules give bitwise identical results.
+    const int pairs = resident_pairs<256, EPI_STORE, 4>(sms);
+    const int units[3] = {a4.pr.num_units, a5.pr.num_units, a6.pr.num_units};
+    const int cost[3] = {a4.pr.kb_end - a4.pr.kb_begin + EPI_KB, a5.pr.kb_end - a5.pr.kb_begin + EPI_KB,
+                         a6.pr.kb_end - a6.pr.kb_begin + EPI_KB};
+    int split[3] = {pairs, pairs, pairs};
+    const BwdSchedule mode = bwd_schedule();
+    bool overlap = false;
+    if (mode != BwdSchedule::Serial && pairs >= 3) {
+        const long long side = split_pairs(pairs, 3, units, cost, split);
+        overlap = mode == BwdSchedule::Overlap || side * 100 <= serial_makespan(pairs, 3, units, cost) * 94;
+    }
+    if (overlap) {
+        std::lock_guard<std::mutex> lock(side_stream_mutex());
+        SideStreams* ss = side_streams(s);
+        if (ss != nullptr) {
+            bool ok = cudaEventRecord(ss->fork, s) == cudaSuccess &&
+                      cudaStreamWaitEvent(ss->s[0], ss->fork, 0) == cudaSuccess &&
+                      cudaStreamWaitEvent(ss->s[1], ss->fork, 0) == cudaSuccess;
+            if (!ok) return MP_ERR_CUDA;
+            ok = launch_gemm_tc<256, EPI_STORE, 4>(m4, a4, sms, s, split[0]) == cudaSuccess;
+            ok = launch_gemm_tc<256, EPI_STORE, 4>(m5, a5, sms, ss->s[0], split[1]) == cudaSuccess && ok;
+            ok = launch_gemm_tc<256, EPI_STORE, 4>(m6, a6, sms, ss->s[1], split[2]) == cudaSuccess && ok;
+            // Join even after a failed launch, so the caller's stream never runs ahead of the side streams.
+            for (int i = 0; i < 2; ++i)
+                ok = cudaEventRecord(ss->join[i], ss->s[i]) == cudaSuccess &&
+                     cudaStreamWaitEvent(s, ss->join[i], 0) == cudaSuccess && ok;
+            return ok ? MP_OK : MP_ERR_CUDA;
+        }
+    }
+    if (launch_gemm_tc<256, EPI_STORE, 4>(m4, a4, sms, s) != cudaSuccess ||
+        launch_gemm_tc<256, EPI_STORE, 4>(m5, a5, sms, s) != cudaSuccess ||
+        launch_gemm_tc<256, EPI_STORE, 4>(m6, a6, sms, s) != cudaSuccess)
+        return MP_ERR_CUDA;
     return MP_OK;
 }
