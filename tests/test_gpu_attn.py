@@ -42,6 +42,8 @@ def _run(inp, b, s, heads, t):
     (1, 512, 384, 4, 4),      # d = 96, four tiles (causal skipping and the diagonal)
     (3, 128, 128, 2, 1),      # d = 64, one tile
     (2, 384, 256, 4, 2),      # d = 64
+    (8, 1024, 512, 8, 2),     # d = 64, 512 work items: several per CTA of the persistent grid
+    (6, 768, 768, 8, 4),      # d = 96, 288 work items of 1..6 key tiles
 ])
 def test_attn_matches_oracle(b, s, h, heads, t):
     inp = _inputs(b, s, h, seed=10000 + s + h)
