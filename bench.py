@@ -375,6 +375,51 @@ def time_next_rows(step, reps, flush):
             "attn_fwd": attn}
 
 
+def time_torch_context(step, reps, flush):
+    """The step's two parts as a plain PyTorch composition on cuBLAS, on the same device
+    tensors, for context only (never part of `value`): Z = GeLU(X A) B, erf form, with its
+    backward through autograd (dX, dA, dB), unsharded; and the unfused loss, logits = X E^T
+    materialised, then fp32 cross-entropy over the valid vocabulary. Median of `reps`, L2
+    flushed before each."""
+    import torch
+    import torch.nn.functional as F
+    d = step.d
+    X, A, B, dZ = d["X"], d["A"], d["B"], d["dZ"]
+    Xc, E, tgt = d["Xc"], d["E"], d["target"].long()
+    v_valid = CE["v_valid"]
+
+    def mlp():
+        Xr, Ar, Br = (t.detach().requires_grad_(True) for t in (X, A, B))
+        Z = F.gelu(Xr @ Ar, approximate="none") @ Br
+        Z.backward(dZ)
+
+    def ce():
+        logits = (Xc @ E.t())[:, :v_valid].float()
+        return F.cross_entropy(logits, tgt, reduction="none")
+
+    def med(fn):
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ts.sort()
+        return ts[len(ts) // 2]
+
+    mlp_ms, ce_ms = med(mlp), med(ce)
+    torch.cuda.empty_cache()
+    return {"mlp_fwd_bwd_ms": mlp_ms, "mlp_tflops": mlp_flop() / (mlp_ms * 1e-3) / 1e12,
+            "ce_ms": ce_ms, "ce_tflops": ce_flop() / (ce_ms * 1e-3) / 1e12,
+            "ce_tokens_per_s": CE["T"] / (ce_ms * 1e-3),
+            "note": "PyTorch + cuBLAS composition of the same step (context only): F.gelu(X@A)@B with "
+                    "autograd backward; (X@E^T)[:, :v_valid] in fp32 then F.cross_entropy"}
+
+
 def time_e2e(step, steps, warmup):
     """The step through the same C-ABI calls with every input copied in from pinned host
     memory and every result (Z, dX, dA, dB, loss) copied back, all inside the timed
@@ -526,6 +571,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
     ap.add_argument("--no-next-rows", action="store_true", help="skip the rows measured beside the step")
+    ap.add_argument("--no-context", action="store_true",
+                    help="skip the PyTorch/cuBLAS composition timed beside the step for context")
     ap.add_argument("--sweep", action="store_true",
                     help="time MLP fwd+bwd and the fused CE at every point of the layer sweep (one JSON line each)")
     ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "mlp", "attn"), default="none",
@@ -577,6 +624,7 @@ def main(argv=None):
 
     breakdown = time_breakdown(step, 9, flush)
     next_rows = None if args.no_next_rows else time_next_rows(step, 9, flush)
+    context = None if args.no_context else time_torch_context(step, 9, flush)
     peaks, peak_src = load_peaks()
     ce_avg_ms = sum(ce_ms) / len(ce_ms)
     ce_achieved = ce_flop() / (ce_avg_ms * 1e-3) / 1e12
@@ -613,6 +661,7 @@ def main(argv=None):
             "ce_tflops": ce_flop() / ((breakdown["ce_partials"] + breakdown["ce_combine"]) * 1e-3) / 1e12,
             "breakdown_ms": breakdown,
             "next_rows": next_rows,
+            "torch_context": context,
             "roofline": {"kernel": "mp_vocab_ce_partials (logit GEMM + online LSE epilogue)", "bound": "tensor",
                          "achieved": ce_achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                          "frac": ce_achieved / peaks["bf16_tflops_sustained"],
