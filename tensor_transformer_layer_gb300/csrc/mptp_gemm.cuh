@@ -124,7 +124,7 @@ struct GemmCfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BNH * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr uint32_t TMEM_COLS = 2 * BN;
+    static constexpr uint32_t TMEM_COLS = BN <= 128 ? 256 : 512;  // two accumulators, power of two
     static constexpr int STG_BYTES = (EPI == EPI_CE) ? 0 : NE * STG_BYTES_PER_WARP;
     static constexpr int MAX_STAGES = 8;
     static constexpr int FIT_STAGES = static_cast<int>((SMEM_LIMIT - 1024 - 512 - STG_BYTES) / STAGE_BYTES);
@@ -133,7 +133,8 @@ struct GemmCfg {
     static constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + STG_BYTES + 8 * NUM_BARS + 16;
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory per block");
     static_assert(STAGES >= 4, "pipeline depth");
-    static_assert(BN == 128 || BN == 256, "pair tile width");
+    static_assert(BN == 128 || BN == 224 || BN == 256, "pair tile width");
+    static_assert(BN != 224 || NE == 4, "224-wide tiles: four epilogue warps (7 column chunks each)");
     static_assert(NE == 4 || NE == 8, "4 or 8 epilogue warps");
     static_assert(EPI != EPI_CE || NE == 4, "cross-entropy epilogue keeps one thread per row");
     static_assert(EPI != EPI_ACC || NE == 4, "accumulating epilogue uses four warps");
@@ -619,14 +620,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
 #pragma unroll 1
                 for (int cc = 0; cc < MY_CHUNKS; cc += 2) {
                     tmem_ld_wait(ra);
-                    issue(cc + 1, rb, ub);
-                    finish(cc, ra, ua);
-                    tmem_ld_wait(rb);
-                    if (cc + 2 < MY_CHUNKS)
-                        issue(cc + 2, ra, ua);
+                    if (cc + 1 < MY_CHUNKS)
+                        issue(cc + 1, rb, ub);
                     else
                         release();
-                    finish(cc + 1, rb, ub);
+                    finish(cc, ra, ua);
+                    if (cc + 1 < MY_CHUNKS) {
+                        tmem_ld_wait(rb);
+                        if (cc + 2 < MY_CHUNKS)
+                            issue(cc + 2, ra, ua);
+                        else
+                            release();
+                        finish(cc + 1, rb, ub);
+                    }
                 }
             }
             if (!ok) break;
@@ -690,6 +696,7 @@ inline cudaError_t launch_gemm_tc(const TmapSet& maps, const GemmArgs& args, int
                                   int max_pairs = 0) {
     using Cfg = GemmCfg<BN, EPI, NE>;
     auto kern = gemm_tc_kernel<BN, EPI, NE>;
+    if (BN % 128 != 0 && args.pr.b_mn) return cudaErrorInvalidValue;  // MN-major B needs 64-column boxes per CTA
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_BYTES));
     if (e != cudaSuccess) return e;

@@ -63,6 +63,13 @@ static BwdSchedule bwd_schedule() {
 // Cost of one output tile in K-block times: its K blocks plus about two for the epilogue.
 constexpr int EPI_KB = 2;
 
+// Tile width of K4 (dX = dU A^T, N = h, B operand K-major). 224-wide tiles cut h = 3072
+// into 14 column units instead of 12, so T = 4096 gives 224 units: 2.95 rounds of 76 CTA
+// pairs, against 2.53 rounds of 256-wide tiles whose last round leaves half the pairs idle.
+#ifndef MPTP_K4_BN
+#define MPTP_K4_BN 224
+#endif
+
 static GemmArgs launch_args(uint32_t* status) {
     GemmArgs a{};
     a.tiles_per_unit = 1;
@@ -151,11 +158,11 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
     // shard i are [i*f/t, (i+1)*f/t) / BK, visited for i = 0..t-1 in order (the f sum).
     const int fs = f / t;
     TmapSet m4{};
-    if (!make_tmap_bf16(&m4.a, dU_ws, f, T, f, 64, BM) || !make_tmap_bf16(&m4.b, A, f, h, f, 64, 128) ||
+    if (!make_tmap_bf16(&m4.a, dU_ws, f, T, f, 64, BM) || !make_tmap_bf16(&m4.b, A, f, h, f, 64, MPTP_K4_BN / 2) ||
         !make_tmap_bf16_out(&m4.o0, dX, h, T, h))
         return MP_ERR_CUDA;
     GemmArgs a4 = launch_args(d_status);
-    a4.pr = problem(T, h, 256, 0 * (fs / BK), t * (fs / BK), false, false, Tb * f, hb * f);
+    a4.pr = problem(T, h, MPTP_K4_BN, 0 * (fs / BK), t * (fs / BK), false, false, Tb * f, hb * f);
 
     // K5a: dA = X^T dU (M = h, N = f, K = T).  Both operands MN-major.
     TmapSet m5{};
@@ -194,7 +201,7 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
                       cudaStreamWaitEvent(ss->s[0], ss->fork, 0) == cudaSuccess &&
                       cudaStreamWaitEvent(ss->s[1], ss->fork, 0) == cudaSuccess;
             if (!ok) return MP_ERR_CUDA;
-            ok = launch_gemm_tc<256, EPI_STORE, 4>(m4, a4, sms, s, split[0]) == cudaSuccess;
+            ok = launch_gemm_tc<MPTP_K4_BN, EPI_STORE, 4>(m4, a4, sms, s, split[0]) == cudaSuccess;
             ok = launch_gemm_tc<256, EPI_STORE, 4>(m5, a5, sms, ss->s[0], split[1]) == cudaSuccess && ok;
             ok = launch_gemm_tc<256, EPI_STORE, 4>(m6, a6, sms, ss->s[1], split[2]) == cudaSuccess && ok;
             // Join even after a failed launch, so the caller's stream never runs ahead of the side streams.
@@ -204,7 +211,7 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
             return ok ? MP_OK : MP_ERR_CUDA;
         }
     }
-    if (launch_gemm_tc<256, EPI_STORE, 4>(m4, a4, sms, s) != cudaSuccess ||
+    if (launch_gemm_tc<MPTP_K4_BN, EPI_STORE, 4>(m4, a4, sms, s) != cudaSuccess ||
         launch_gemm_tc<256, EPI_STORE, 4>(m5, a5, sms, s) != cudaSuccess ||
         launch_gemm_tc<256, EPI_STORE, 4>(m6, a6, sms, s) != cudaSuccess)
         return MP_ERR_CUDA;
