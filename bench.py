@@ -60,6 +60,29 @@ def step_flop():
     return mlp_flop() + ce_flop()
 
 
+# Dense bf16 tensor-core rate of one sm_103 SM (tcgen05 kind::f16, FLOP per clock).
+BF16_FLOP_PER_CLK_PER_SM = 8192
+
+
+def peak_table(value, mlp_tf, ce_tf, peaks, peak_src, dev, clocks):
+    """Fractions of the three denominators: the theoretical dense bf16 peak (SMs x per-SM
+    rate x the maximum SM clock seen by nvidia-smi, else the device's), and the measured
+    burst and sustained bf16 GEMM rates."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    mhz = (clocks or {}).get("sm_max_mhz")
+    if not mhz:
+        mhz = getattr(props, "clock_rate", 0) / 1000.0 or 2070.0
+    theo = props.multi_processor_count * BF16_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12
+    out = {"theoretical_dense_bf16": {"tflops": theo, "sms": props.multi_processor_count,
+                                      "flop_per_clk_per_sm": BF16_FLOP_PER_CLK_PER_SM, "clock_mhz": mhz}}
+    for name, key in (("measured_burst", "bf16_tflops"), ("measured_sustained", "bf16_tflops_sustained")):
+        out[name] = {"tflops": peaks[key], "source": peak_src}
+    for d in out.values():
+        d["frac"] = {"step": value / d["tflops"], "mlp_fwd_bwd": mlp_tf / d["tflops"], "ce": ce_tf / d["tflops"]}
+    return out
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -261,6 +284,24 @@ def time_device(step, steps, warmup, flush):
     return step_ms, ce_ms
 
 
+def event_median(fn, reps, flush):
+    """Median device time (ms) of fn() over `reps` calls, L2 flushed before each. All calls
+    are enqueued before one synchronize, so the host's launch time of a short call is not
+    counted as device time."""
+    import torch
+    evs = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    ts = sorted(a.elapsed_time(b) for a, b in evs)
+    return ts[len(ts) // 2]
+
+
 def time_breakdown(step, reps, flush):
     """Per-call device times (ms, median) of the step's four C-ABI calls."""
     import torch
@@ -274,20 +315,7 @@ def time_breakdown(step, reps, flush):
         "ce_combine": lambda: mp.mp_vocab_ce_combine(step.ws, d["target"], d["loss"], v_pad=CE["v_pad"],
                                                      v_valid=CE["v_valid"], t=CE["t"]),
     }
-    out = {}
-    for name, fn in calls.items():
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        ts.sort()
-        out[name] = round(ts[len(ts) // 2], 4)
-    return out
+    return {name: round(event_median(fn, reps, flush), 4) for name, fn in calls.items()}
 
 
 def time_next_rows(step, reps, flush):
@@ -304,33 +332,13 @@ def time_next_rows(step, reps, flush):
     fn = lambda: mp.mp_vocab_ce_bwd(d["Xc"], d["E"], d["target"], d["loss"], dloss, dXc, dE, wsb, v_valid=v_valid,
                                     t=t, d_status=step.status)
     fn()
-    ts = []
-    for _ in range(reps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        torch.cuda.synchronize()
-        ts.append(a.elapsed_time(b))
-    ts.sort()
-    ms = ts[len(ts) // 2]
+    ms = event_median(fn, reps, flush)
     step.check_status()
     # vocab-parallel input embedding of the same T tokens (ids = the targets)
     emb = torch.empty(T, h, dtype=torch.bfloat16, device=d["Xc"].device)
     efn = lambda: mp.mp_vocab_embed(d["target"], d["E"], emb, v_valid=v_valid, t=t, d_status=step.status)
     efn()
-    ets = []
-    for _ in range(reps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        efn()
-        b.record()
-        torch.cuda.synchronize()
-        ets.append(a.elapsed_time(b))
-    ets.sort()
-    ems = ets[len(ets) // 2]
+    ems = event_median(efn, reps, flush)
     ebytes = 2.0 * T * h * 2 + 4.0 * T   # read T rows of E, write T rows, read the ids
     peaks, peak_src = load_peaks()
     embed = {"ms": ems, "gbs": ebytes / (ems * 1e-3) / 1e9, "bytes": ebytes,
@@ -348,17 +356,7 @@ def time_next_rows(step, reps, flush):
     afn = lambda: mp.mp_attn_fwd(ax, awqkv, awo, aout, aqkv, ao, b=ab, s=as_, heads=aheads, t=at,
                                  d_status=step.status)
     afn()
-    ats = []
-    for _ in range(reps):
-        flush.zero_()
-        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        afn()
-        b_.record()
-        torch.cuda.synchronize()
-        ats.append(a.elapsed_time(b_))
-    ats.sort()
-    ams = ats[len(ats) // 2]
+    ams = event_median(afn, reps, flush)
     hd = ah // aheads
     attn_core = 4.0 * ab * aheads * hd * as_ * (as_ + 1) / 2     # QK^T and PV over the causal pairs
     attn_flop = 2.0 * aT * ah * 3 * ah + attn_core + 2.0 * aT * ah * ah
@@ -397,21 +395,9 @@ def time_torch_context(step, reps, flush):
         logits = (Xc @ E.t())[:, :v_valid].float()
         return F.cross_entropy(logits, tgt, reduction="none")
 
-    def med(fn):
-        fn()
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        ts.sort()
-        return ts[len(ts) // 2]
-
-    mlp_ms, ce_ms = med(mlp), med(ce)
+    mlp()
+    ce()
+    mlp_ms, ce_ms = event_median(mlp, reps, flush), event_median(ce, reps, flush)
     torch.cuda.empty_cache()
     return {"mlp_fwd_bwd_ms": mlp_ms, "mlp_tflops": mlp_flop() / (mlp_ms * 1e-3) / 1e12,
             "ce_ms": ce_ms, "ce_tflops": ce_flop() / (ce_ms * 1e-3) / 1e12,
@@ -673,6 +659,9 @@ def main(argv=None):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(),
             "pct_of_measured_bf16_sustained": value / peaks["bf16_tflops_sustained"],
+            "pct_of_peak": peak_table(value, mlp_flop() / (mlp_ms * 1e-3) / 1e12,
+                                      ce_flop() / ((breakdown["ce_partials"] + breakdown["ce_combine"]) * 1e-3) / 1e12,
+                                      peaks, peak_src, dev, clocks),
             "mlp_fwd_bwd_tflops": mlp_flop() / (mlp_ms * 1e-3) / 1e12,
             "ce_tokens_per_s": CE["T"] / ((breakdown["ce_partials"] + breakdown["ce_combine"]) * 1e-3),
             "ce_tflops": ce_flop() / ((breakdown["ce_partials"] + breakdown["ce_combine"]) * 1e-3) / 1e12,
@@ -711,17 +700,7 @@ def run_sweep(dev, reps, warmup):
     def med(fn):
         for _ in range(warmup):
             fn()
-        ts = []
-        for _ in range(reps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record()
-            fn()
-            b.record()
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b))
-        ts.sort()
-        return ts[len(ts) // 2]
+        return event_median(fn, reps, flush)
 
     for h in (1536, 1920, 2304, 3072):
         f = 4 * h

@@ -44,6 +44,8 @@
 
 #include <cuda_bf16.h>
 
+#include <cstdlib>
+
 #include "mptp_ptx.cuh"
 
 namespace mptp {
@@ -690,6 +692,12 @@ inline int resident_pairs(int num_sms) {
     return clusters;
 }
 
+// MPTP_BALANCE_PAIRS=0 launches every resident pair even when fewer give the same rounds.
+inline bool balance_pairs() {
+    const char* v = std::getenv("MPTP_BALANCE_PAIRS");
+    return !(v != nullptr && v[0] == '0');
+}
+
 // Host-side launcher: grid = 2 x min(units, resident pairs, max_pairs if > 0), one CTA per SM.
 template <int BN, int EPI, int NE>
 inline cudaError_t launch_gemm_tc(const TmapSet& maps, const GemmArgs& args, int num_sms, cudaStream_t stream,
@@ -702,7 +710,13 @@ inline cudaError_t launch_gemm_tc(const TmapSet& maps, const GemmArgs& args, int
     if (e != cudaSuccess) return e;
     int pairs = resident_pairs<BN, EPI, NE>(num_sms);
     if (max_pairs > 0 && max_pairs < pairs) pairs = max_pairs;
-    const int use = args.pr.num_units < pairs ? args.pr.num_units : pairs;
+    int use = args.pr.num_units < pairs ? args.pr.num_units : pairs;
+    // As few pairs as give the same number of rounds of units: the same time, and the idle
+    // SMs leave power headroom to the busy ones under the board's power cap.
+    if (use > 0 && balance_pairs()) {
+        const int rounds = (args.pr.num_units + use - 1) / use;
+        use = (args.pr.num_units + rounds - 1) / rounds;
+    }
     if (use <= 0) return cudaSuccess;
     kern<<<2 * use, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(maps, args);
     return cudaGetLastError();
