@@ -66,6 +66,7 @@ enum EpiKind : int {
     EPI_CE = 3,     // per-row online max / sum-exp / target logit over the unit
     EPI_DZ = 4,     // out0 = bf16(dloss * (exp(acc - lse) - [col == target])), 0 on padding columns
     EPI_ACC = 5,    // fp32 accumulation across launches into `acc`; the last launch stores bf16 out0
+    EPI_STORE_G = 6,  // out0 = bf16(acc) stored from registers (no staging: one more pipeline stage)
 };
 
 enum AccMode : int {
@@ -103,6 +104,9 @@ struct GemmArgs {
     float* acc;
     long long ld_acc;
     int acc_mode;
+    // direct-store epilogue
+    __nv_bfloat16* out0;
+    long long ld_out0;
     uint32_t* status;         // nullable
     unsigned long long budget_ns;
 };
@@ -127,7 +131,7 @@ struct GemmCfg {
     static constexpr int B_BYTES = BNH * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TMEM_COLS = BN <= 128 ? 256 : 512;  // two accumulators, power of two
-    static constexpr int STG_BYTES = (EPI == EPI_CE) ? 0 : NE * STG_BYTES_PER_WARP;
+    static constexpr int STG_BYTES = (EPI == EPI_CE || EPI == EPI_STORE_G) ? 0 : NE * STG_BYTES_PER_WARP;
     static constexpr int MAX_STAGES = 8;
     static constexpr int FIT_STAGES = static_cast<int>((SMEM_LIMIT - 1024 - 512 - STG_BYTES) / STAGE_BYTES);
     static constexpr int STAGES = FIT_STAGES < MAX_STAGES ? FIT_STAGES : MAX_STAGES;
@@ -309,7 +313,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&maps.a);
         prefetch_tensormap(&maps.b);
-        if (EPI != EPI_CE) prefetch_tensormap(&maps.o0);
+        if (EPI != EPI_CE && EPI != EPI_STORE_G) prefetch_tensormap(&maps.o0);
         if (EPI == EPI_GELU && args.has_out1) prefetch_tensormap(&maps.o1);
     }
     if (warp == 1) {
@@ -386,6 +390,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                 const uint32_t a_lbo = a_mn ? 8192u : 16u, b_lbo = b_mn ? 8192u : 16u;
                 const uint64_t a_kstep = a_mn ? (2048u >> 4) : (32u >> 4);
                 const uint64_t b_kstep = b_mn ? (2048u >> 4) : (32u >> 4);
+                const uint64_t ad_base = make_sdesc_sw128(smem_u32(sA), a_lbo, 1024);
+                const uint64_t bd_base = make_sdesc_sw128(smem_u32(sB), b_lbo, 1024);
                 for (int nt = 0; nt < args.tiles_per_unit && ok; ++nt, ++tcount) {
                     const uint32_t buf = tcount & 1u;
                     const uint32_t tph = (tcount >> 1) & 1u;
@@ -395,18 +401,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                     }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + buf * BN;
+                    // The issuing thread is on the critical path: one stage's four MMAs take 512
+                    // tensor cycles, and everything else it does per stage must fit beside them.
+                    // Stage descriptors are the stage-0 ones advanced in their address field.
                     for (int kb = p.kb_begin; kb < p.kb_end; ++kb) {
-                        if (!wait_bounded(&full_bar[stage], phase, ctl)) {
+                        if (!mbar_test_wait(&full_bar[stage], phase) && !wait_bounded(&full_bar[stage], phase, ctl)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t ad0 = make_sdesc_sw128(smem_u32(sA + stage * Cfg::A_BYTES), a_lbo, 1024);
-                        const uint64_t bd0 = make_sdesc_sw128(smem_u32(sB + stage * Cfg::B_BYTES), b_lbo, 1024);
+                        const uint64_t ad0 = ad_base + static_cast<uint64_t>(stage) * (Cfg::A_BYTES >> 4);
+                        const uint64_t bd0 = bd_base + static_cast<uint64_t>(stage) * (Cfg::B_BYTES >> 4);
+                        umma_bf16_pair(d_tmem, ad0, bd0, idesc, kb > p.kb_begin ? 1u : 0u);
 #pragma unroll
-                        for (int k = 0; k < BK / UMMA_K; ++k)
-                            umma_bf16_pair(d_tmem, ad0 + k * a_kstep, bd0 + k * b_kstep, idesc,
-                                           (kb > p.kb_begin || k > 0) ? 1u : 0u);
+                        for (int k = 1; k < BK / UMMA_K; ++k)
+                            umma_bf16_pair_acc(d_tmem, ad0 + k * a_kstep, bd0 + k * b_kstep, idesc);
                         umma_commit_pair_multicast(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
                         if (++stage == STAGES) {
                             stage = 0;
@@ -544,6 +553,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                             pk[j] = pack_bf16x2(g[0], g[1]);
                         }
                         stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
+                    } else if constexpr (EPI == EPI_STORE_G) {
+                        // The row's 32 columns are 64 contiguous bytes: four 16-byte stores.
+                        if (row_ok) {
+                            uint4* dst = reinterpret_cast<uint4*>(args.out0 + static_cast<long long>(row) * args.ld_out0 +
+                                                                  col0);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                dst[j] = make_uint4(
+                                    pack_bf16x2(__uint_as_float(r[8 * j]), __uint_as_float(r[8 * j + 1])),
+                                    pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
+                                    pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
+                                    pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
+                        }
                     } else if constexpr (EPI == EPI_ACC) {
                         if (args.acc_mode == ACC_ONLY || args.acc_mode == ACC_LAST) {
                             float v[32];
@@ -648,7 +670,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
             }
         }
         // All of this warp's TMA stores must have landed before the kernel ends.
-        if (EPI != EPI_CE && lane == 0) bulk_wait_group<0>();
+        if (EPI != EPI_CE && EPI != EPI_STORE_G && lane == 0) bulk_wait_group<0>();
     }
 
     // ---------------- teardown ----------------

@@ -63,6 +63,12 @@ static BwdSchedule bwd_schedule() {
 // Cost of one output tile in K-block times: its K blocks plus about two for the epilogue.
 constexpr int EPI_KB = 2;
 
+// Epilogue of the plain-store GEMMs (K2, K4, K5): bf16 rows stored from registers, which
+// leaves room for a seventh pipeline stage.
+#ifndef MPTP_STORE_EPI
+#define MPTP_STORE_EPI EPI_STORE_G
+#endif
+
 // Tile width of K4 (dX = dU A^T, N = h, B operand K-major). 224-wide tiles cut h = 3072
 // into 14 column units instead of 12, so T = 4096 gives 224 units: 2.95 rounds of 76 CTA
 // pairs, against 2.53 rounds of 256-wide tiles whose last round leaves half the pairs idle.
@@ -116,7 +122,9 @@ extern "C" mp_status mp_mlp_fwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
         return MP_ERR_CUDA;
     GemmArgs a2 = launch_args(d_status);
     a2.pr = problem(T, h, 256, 0 * (fs / BK), t * (fs / BK), false, true, Tb * f, hb * f);
-    if (launch_gemm_tc<256, EPI_STORE, 4>(m2, a2, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+    a2.out0 = reinterpret_cast<__nv_bfloat16*>(Z);
+    a2.ld_out0 = h;
+    if (launch_gemm_tc<256, MPTP_STORE_EPI, 4>(m2, a2, sms, s) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
 
@@ -163,6 +171,8 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
         return MP_ERR_CUDA;
     GemmArgs a4 = launch_args(d_status);
     a4.pr = problem(T, h, MPTP_K4_BN, 0 * (fs / BK), t * (fs / BK), false, false, Tb * f, hb * f);
+    a4.out0 = reinterpret_cast<__nv_bfloat16*>(dX);
+    a4.ld_out0 = h;
 
     // K5a: dA = X^T dU (M = h, N = f, K = T).  Both operands MN-major.
     TmapSet m5{};
@@ -171,6 +181,8 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
         return MP_ERR_CUDA;
     GemmArgs a5 = launch_args(d_status);
     a5.pr = problem(h, f, 256, 0, ceil_div(T, BK), true, true, Tb * h, Tb * f);
+    a5.out0 = reinterpret_cast<__nv_bfloat16*>(dA);
+    a5.ld_out0 = f;
 
     // K5b: dB = Y^T dZ (M = f, N = h, K = T).  Both operands MN-major.
     TmapSet m6{};
@@ -179,10 +191,12 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
         return MP_ERR_CUDA;
     GemmArgs a6 = launch_args(d_status);
     a6.pr = problem(f, h, 256, 0, ceil_div(T, BK), true, true, Tb * f, Tb * h);
+    a6.out0 = reinterpret_cast<__nv_bfloat16*>(dB);
+    a6.ld_out0 = h;
 
     // Every output tile is computed by the same K-loop whichever pairs run it, so both
     // schedules give bitwise identical results.
-    const int pairs = resident_pairs<256, EPI_STORE, 4>(sms);
+    const int pairs = resident_pairs<256, MPTP_STORE_EPI, 4>(sms);
     const int units[3] = {a4.pr.num_units, a5.pr.num_units, a6.pr.num_units};
     const int cost[3] = {a4.pr.kb_end - a4.pr.kb_begin + EPI_KB, a5.pr.kb_end - a5.pr.kb_begin + EPI_KB,
                          a6.pr.kb_end - a6.pr.kb_begin + EPI_KB};
@@ -201,9 +215,9 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
                       cudaStreamWaitEvent(ss->s[0], ss->fork, 0) == cudaSuccess &&
                       cudaStreamWaitEvent(ss->s[1], ss->fork, 0) == cudaSuccess;
             if (!ok) return MP_ERR_CUDA;
-            ok = launch_gemm_tc<MPTP_K4_BN, EPI_STORE, 4>(m4, a4, sms, s, split[0]) == cudaSuccess;
-            ok = launch_gemm_tc<256, EPI_STORE, 4>(m5, a5, sms, ss->s[0], split[1]) == cudaSuccess && ok;
-            ok = launch_gemm_tc<256, EPI_STORE, 4>(m6, a6, sms, ss->s[1], split[2]) == cudaSuccess && ok;
+            ok = launch_gemm_tc<MPTP_K4_BN, MPTP_STORE_EPI, 4>(m4, a4, sms, s, split[0]) == cudaSuccess;
+            ok = launch_gemm_tc<256, MPTP_STORE_EPI, 4>(m5, a5, sms, ss->s[0], split[1]) == cudaSuccess && ok;
+            ok = launch_gemm_tc<256, MPTP_STORE_EPI, 4>(m6, a6, sms, ss->s[1], split[2]) == cudaSuccess && ok;
             // Join even after a failed launch, so the caller's stream never runs ahead of the side streams.
             for (int i = 0; i < 2; ++i)
                 ok = cudaEventRecord(ss->join[i], ss->s[i]) == cudaSuccess &&
@@ -211,9 +225,9 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
             return ok ? MP_OK : MP_ERR_CUDA;
         }
     }
-    if (launch_gemm_tc<MPTP_K4_BN, EPI_STORE, 4>(m4, a4, sms, s) != cudaSuccess ||
-        launch_gemm_tc<256, EPI_STORE, 4>(m5, a5, sms, s) != cudaSuccess ||
-        launch_gemm_tc<256, EPI_STORE, 4>(m6, a6, sms, s) != cudaSuccess)
+    if (launch_gemm_tc<MPTP_K4_BN, MPTP_STORE_EPI, 4>(m4, a4, sms, s) != cudaSuccess ||
+        launch_gemm_tc<256, MPTP_STORE_EPI, 4>(m5, a5, sms, s) != cudaSuccess ||
+        launch_gemm_tc<256, MPTP_STORE_EPI, 4>(m6, a6, sms, s) != cudaSuccess)
         return MP_ERR_CUDA;
     return MP_OK;
 }
