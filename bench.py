@@ -94,10 +94,17 @@ def load_peaks():
 
 
 def kernel_source_hash():
+    """sha256[:16] of the kernel sources with comments and blank lines removed, so that a
+    recorded profile stays valid across comment-only edits."""
+    import re
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "tensor_transformer_layer_gb300", "csrc", name), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "tensor_transformer_layer_gb300", "csrc", name)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        text = "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+        h.update(text.encode())
     return h.hexdigest()[:16]
 
 

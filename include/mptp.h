@@ -108,6 +108,12 @@ MP_API mp_status mp_mlp_fwd(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B
  *   dU_ws [T,f]                                             workspace (caller-owned);
  *                                                           holds dU (bf16) on return
  *   Size rules as mp_mlp_fwd.
+ *   Streams: everything is ordered on `stream`. When its estimated makespan is at
+ *   least 6 % shorter, dX, dA and dB run side by side on disjoint CTA pairs, dX on
+ *   `stream` and dA, dB on two internal side streams of the device that wait on an
+ *   event recorded on `stream` and are joined back to it before the call returns
+ *   (also inside a CUDA graph capture, once the side streams exist). The results are
+ *   bitwise the same either way. MPTP_BWD_SCHEDULE=serial|overlap forces one of them.
  */
 MP_API mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B,
                      const mp_bf16* U, const mp_bf16* Y, const mp_bf16* dZ,

@@ -10,18 +10,21 @@
 // CTA's 128 x BN accumulator into that CTA's TMEM. Per SM this halves the B
 // traffic, so a stage is 32 KB (BN = 256) and the ring holds 6 stages.
 //
-// Grid = 2 x min(work units, co-resident pairs); 64 + 32*NE threads per CTA:
+// Grid = 2 x the fewest co-resident pairs that finish the units in the fewest
+// rounds; 64 + 32*NE threads per CTA:
 //   warp 0      TMA producer (one lane) in each CTA: its A and B halves per
 //               stage, completion signalled on the leader's `full` barrier.
 //   warp 1      TMEM allocator (whole warp, both CTAs) and, in the leader only,
 //               the MMA issuer (one lane): 4 x tcgen05.mma (K = 16) per stage into
-//               one of two TMEM accumulators (2*BN fp32 columns per CTA); its
+//               one of two TMEM accumulators (BN fp32 columns each per CTA); its
 //               commits arrive on the `empty` / `tmem full` barriers of both CTAs.
 //   warps 2..   NE epilogue warps (4 or 8) in each CTA: tcgen05.ld 32 rows x 32
 //               columns (TMEM lane quarter = warp % 4, thread = output row; with 8
 //               warps two warps share a quarter and split the columns), fused math,
-//               then bf16 rows staged in a 64-byte-swizzled shared box per warp and
-//               written by TMA stores (32x32 boxes), or cross-entropy partials. An
+//               then bf16 rows either stored straight from registers (plain store,
+//               which leaves room for one more pipeline stage) or staged in a
+//               64-byte-swizzled shared box per warp and written by TMA stores (32x32
+//               boxes), or cross-entropy partials. An
 //               accumulator is handed back (to the leader) as soon as its last
 //               columns are in registers, so it overlaps the next tile's MMAs.
 //
