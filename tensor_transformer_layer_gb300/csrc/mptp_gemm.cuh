@@ -69,8 +69,16 @@ enum EpiKind : int {
     EPI_CE = 3,     // per-row online max / sum-exp / target logit over the unit
     EPI_DZ = 4,     // out0 = bf16(dloss * (exp(acc - lse) - [col == target])), 0 on padding columns
     EPI_ACC = 5,    // fp32 accumulation across launches into `acc`; the last launch stores bf16 out0
-    EPI_STORE_G = 6,  // out0 = bf16(acc) stored from registers (no staging: one more pipeline stage)
+    EPI_STORE_G = 6,  // as EPI_STORE, GELU, DGELU, but rows stored from registers: no staging
+    EPI_GELU_G = 7,   // boxes, so the shared memory they took holds one more pipeline stage
+    EPI_DGELU_G = 8,
 };
+
+// Register-store (direct) form of an epilogue, and the math it shares with the staged form.
+__host__ __device__ constexpr bool epi_direct(int e) { return e == EPI_STORE_G || e == EPI_GELU_G || e == EPI_DGELU_G; }
+__host__ __device__ constexpr int epi_math(int e) {
+    return e == EPI_STORE_G ? EPI_STORE : e == EPI_GELU_G ? EPI_GELU : e == EPI_DGELU_G ? EPI_DGELU : e;
+}
 
 enum AccMode : int {
     ACC_FIRST = 0,  // acc = C
@@ -107,9 +115,11 @@ struct GemmArgs {
     float* acc;
     long long ld_acc;
     int acc_mode;
-    // direct-store epilogue
+    // register-store epilogues: out0 (and for GeLU out1 = U) with their row pitches
     __nv_bfloat16* out0;
     long long ld_out0;
+    __nv_bfloat16* out1;
+    long long ld_out1;
     uint32_t* status;         // nullable
     unsigned long long budget_ns;
 };
@@ -134,7 +144,7 @@ struct GemmCfg {
     static constexpr int B_BYTES = BNH * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TMEM_COLS = BN <= 128 ? 256 : 512;  // two accumulators, power of two
-    static constexpr int STG_BYTES = (EPI == EPI_CE || EPI == EPI_STORE_G) ? 0 : NE * STG_BYTES_PER_WARP;
+    static constexpr int STG_BYTES = (EPI == EPI_CE || epi_direct(EPI)) ? 0 : NE * STG_BYTES_PER_WARP;
     static constexpr int MAX_STAGES = 8;
     static constexpr int FIT_STAGES = static_cast<int>((SMEM_LIMIT - 1024 - 512 - STG_BYTES) / STAGE_BYTES);
     static constexpr int STAGES = FIT_STAGES < MAX_STAGES ? FIT_STAGES : MAX_STAGES;
@@ -316,7 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&maps.a);
         prefetch_tensormap(&maps.b);
-        if (EPI != EPI_CE && EPI != EPI_STORE_G) prefetch_tensormap(&maps.o0);
+        if (EPI != EPI_CE && !epi_direct(EPI)) prefetch_tensormap(&maps.o0);
         if (EPI == EPI_GELU && args.has_out1) prefetch_tensormap(&maps.o1);
     }
     if (warp == 1) {
@@ -486,7 +496,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                 // chunk cc+1 is in flight while chunk cc is computed and stored.
                 auto issue = [&](int cc, uint32_t (&rr)[32], uint32_t (&uu)[16]) {
                     const int c = c_begin + cc;
-                    if constexpr (EPI == EPI_DGELU) {
+                    if constexpr (epi_math(EPI) == EPI_DGELU) {
                         const int col0 = n_blk * BN + c * 32;
                         if (row_ok && col0 < p.N) {
                             const uint4* src = reinterpret_cast<const uint4*>(args.aux + row * args.ld_aux + col0);
@@ -509,25 +519,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                     const int c = c_begin + cc;
                     const int col0 = n_blk * BN + c * 32;
                     if (col0 >= p.N) return;  // ragged N tail (whole 32-column chunks)
-                    if constexpr (EPI == EPI_STORE) {
+                    // One 32-column bf16 row segment: staged and TMA-stored, or (register-store
+                    // forms) 64 contiguous bytes written as four 16-byte stores.
+                    auto emit = [&](const CUtensorMap* map, __nv_bfloat16* out, long long ld, const uint32_t (&pk)[16]) {
+                        if constexpr (epi_direct(EPI)) {
+                            if (row_ok) {
+                                uint4* dst = reinterpret_cast<uint4*>(out + static_cast<long long>(row) * ld + col0);
+#pragma unroll
+                                for (int j = 0; j < 4; ++j)
+                                    dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                            }
+                        } else {
+                            stage_and_store(map, stg, sbuf, lane, pk, col0, row0);
+                        }
+                    };
+                    if constexpr (epi_math(EPI) == EPI_STORE) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                        stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
-                    } else if constexpr (EPI == EPI_GELU) {
+                        emit(tmO0, args.out0, args.ld_out0, pk);
+                    } else if constexpr (epi_math(EPI) == EPI_GELU) {
                         uint32_t pk[16];
                         if (args.has_out1) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
                                 pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                            stage_and_store(&maps.o1, stg, sbuf, lane, pk, col0, row0);
+                            emit(&maps.o1, args.out1, args.ld_out1, pk);
                         }
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             pk[j] = pack_bf16x2(gelu_f(__uint_as_float(r[2 * j])), gelu_f(__uint_as_float(r[2 * j + 1])));
-                        stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
-                    } else if constexpr (EPI == EPI_DGELU) {
+                        emit(tmO0, args.out0, args.ld_out0, pk);
+                    } else if constexpr (epi_math(EPI) == EPI_DGELU) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
@@ -535,7 +559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                             const float g1 = __uint_as_float(r[2 * j + 1]) * gelu_prime_f(bf16_hi(uw[j]));
                             pk[j] = pack_bf16x2(g0, g1);
                         }
-                        stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
+                        emit(tmO0, args.out0, args.ld_out0, pk);
                     } else if constexpr (EPI == EPI_DZ) {
                         // dZ = dloss * (softmax - onehot) on valid columns, 0 on padding.
                         constexpr float LOG2E = 1.4426950408889634f;
@@ -556,19 +580,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                             pk[j] = pack_bf16x2(g[0], g[1]);
                         }
                         stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
-                    } else if constexpr (EPI == EPI_STORE_G) {
-                        // The row's 32 columns are 64 contiguous bytes: four 16-byte stores.
-                        if (row_ok) {
-                            uint4* dst = reinterpret_cast<uint4*>(args.out0 + static_cast<long long>(row) * args.ld_out0 +
-                                                                  col0);
-#pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                dst[j] = make_uint4(
-                                    pack_bf16x2(__uint_as_float(r[8 * j]), __uint_as_float(r[8 * j + 1])),
-                                    pack_bf16x2(__uint_as_float(r[8 * j + 2]), __uint_as_float(r[8 * j + 3])),
-                                    pack_bf16x2(__uint_as_float(r[8 * j + 4]), __uint_as_float(r[8 * j + 5])),
-                                    pack_bf16x2(__uint_as_float(r[8 * j + 6]), __uint_as_float(r[8 * j + 7])));
-                        }
                     } else if constexpr (EPI == EPI_ACC) {
                         if (args.acc_mode == ACC_ONLY || args.acc_mode == ACC_LAST) {
                             float v[32];
@@ -673,7 +684,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
             }
         }
         // All of this warp's TMA stores must have landed before the kernel ends.
-        if (EPI != EPI_CE && EPI != EPI_STORE_G && lane == 0) bulk_wait_group<0>();
+        if (EPI != EPI_CE && !epi_direct(EPI) && lane == 0) bulk_wait_group<0>();
     }
 
     // ---------------- teardown ----------------

@@ -68,6 +68,16 @@ constexpr int EPI_KB = 2;
 #ifndef MPTP_STORE_EPI
 #define MPTP_STORE_EPI EPI_STORE_G
 #endif
+#ifndef MPTP_GELU_EPI
+#define MPTP_GELU_EPI EPI_GELU_G
+#endif
+#ifndef MPTP_DGELU_EPI
+#define MPTP_DGELU_EPI EPI_DGELU_G
+#endif
+// Epilogue warps of K1 and K3.
+#ifndef MPTP_K13_NE
+#define MPTP_K13_NE 4
+#endif
 
 // Tile width of K4 (dX = dU A^T, N = h, B operand K-major). 224-wide tiles cut h = 3072
 // into 14 column units instead of 12, so T = 4096 gives 224 units: 2.95 rounds of 76 CTA
@@ -111,7 +121,11 @@ extern "C" mp_status mp_mlp_fwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
     GemmArgs a1 = launch_args(d_status);
     a1.pr = problem(T, f, 256, 0, h / BK, false, true, Tb * h, hb * f);
     a1.has_out1 = U_save ? 1 : 0;
-    if (launch_gemm_tc<256, EPI_GELU, 8>(m1, a1, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+    a1.out0 = reinterpret_cast<__nv_bfloat16*>(Y);
+    a1.ld_out0 = f;
+    a1.out1 = reinterpret_cast<__nv_bfloat16*>(U_save);
+    a1.ld_out1 = f;
+    if (launch_gemm_tc<256, MPTP_GELU_EPI, MPTP_K13_NE>(m1, a1, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
     // K2: row-parallel GEMM Z = sum_i Y_i B_i; K blocks of shard i are [i*f/t, (i+1)*f/t) / BK,
     // visited for i = 0..t-1 in order, all into the same accumulator (the g sum).
@@ -160,7 +174,9 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
     a3.pr = problem(T, f, 256, 0, h / BK, false, false, Tb * h, fb * h);
     a3.aux = reinterpret_cast<const __nv_bfloat16*>(U);
     a3.ld_aux = f;
-    if (launch_gemm_tc<256, EPI_DGELU, 8>(m3, a3, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+    a3.out0 = reinterpret_cast<__nv_bfloat16*>(dU_ws);
+    a3.ld_out0 = f;
+    if (launch_gemm_tc<256, MPTP_DGELU_EPI, MPTP_K13_NE>(m3, a3, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
     // K4: dX = sum_i dU_i A_i^T.  A operand dU [T,f] (K-major), B operand A [h,f] (K-major); K blocks of
     // shard i are [i*f/t, (i+1)*f/t) / BK, visited for i = 0..t-1 in order (the f sum).
