@@ -250,10 +250,10 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
 
+        // Every lane polls (one warp instruction either way, and no divergent branch).
         auto wait_lane0 = [&](uint64_t* bar, uint32_t parity) -> bool {
-            bool got = true;
-            if (lane == 0) got = wait_bounded(bar, parity, ctl);
-            return __shfl_sync(0xffffffffu, got ? 1 : 0, 0) != 0;
+            const bool got = wait_bounded(bar, parity, ctl);
+            return __all_sync(0xffffffffu, got) != 0;
         };
         uint8_t* prow = sP + g * Cfg::P_BYTES + qrow * 128;
         const int sw = qrow & 7;
