@@ -12,28 +12,28 @@
 //   out = sum_i O_i Wo_i          row-parallel GEMM, shards in ascending order in the K-loop
 //
 // Attention kernel: one CTA per (sequence, head, pair of consecutive 128-query tiles
-// 2p and 2p+1), 320 threads, the longest pairs launched first. The two query tiles
+// 2p and 2p+1), 384 threads, the longest pairs launched first. The two query tiles
 // ("A" = 2p, "B" = 2p+1) share every K and V tile they both need (causal: keys 0..2p for
 // A, 0..2p+1 for B), so each K/V tile is loaded once for 256 queries.
-//   warp 0      TMA producer: both Q tiles once, then K tiles into a ring that runs
-//               ahead and V tiles into a ring of their own. Head width D is loaded as
-//               D/32 boxes of 32 columns with the 64-byte swizzle.
-//   warp 1      TMEM allocator and MMA issuer. TMEM holds S_A, S_B (128 columns each)
-//               and the output accumulators O_A, O_B (D columns, at 256 and 384). Per key
-//               tile j it issues S_A(j+1), S_B(j+1) = Q K_{j+1}^T, then PV_A(j), PV_B(j),
-//               which accumulate P V_j into O in TMEM; the scores of the next tile are
-//               computed while the two softmax groups work on this one, and each group's
-//               softmax overlaps the other group's products.
-//   warps 2..5  softmax of tile A, warps 6..9 of tile B; thread = query row (the TMEM lane
-//               quarter of the warp), all 128 key columns. The score row is read from TMEM
-//               once and the buffer released at once; row max over eight chains. The
-//               running max is raised lazily: only when it grows by more than 2^8 in the
-//               exp2 domain are O (in TMEM) and the row sum rescaled by
+//   warpgroup 0 (64 registers a thread): warp 0 is the TMA producer: both Q tiles once, then
+//               K tiles into a ring that runs ahead and V tiles into a ring of their own
+//               (head width D loaded as D/32 boxes of 32 columns, 64-byte swizzle). Warp 1
+//               allocates TMEM and issues the products: the whole warp runs the issue loop
+//               and one elected lane issues. Warps 2 and 3 only lend their registers.
+//               TMEM holds S_A, S_B (128 columns each) and the output accumulators O_A, O_B
+//               (D columns, at 256 and 384). Per key tile j and query tile g it issues
+//               PV_g(j) (O_g += P_g V_j, P_g read from TMEM) and then S_g(j+1) = Q_g K_{j+1}^T;
+//               while one tile's softmax runs, the tensor core works on the other tile.
+//   warpgroups 1, 2 (216 registers a thread): softmax of tile A and of tile B; thread =
+//               query row (the TMEM lane quarter of the warp), all 128 key columns. The
+//               score row is read from TMEM once; row max over four chains of three-input
+//               maxima. The running max is raised lazily: only when it grows by more than
+//               2^8 in the exp2 domain are O (in TMEM) and the row sum rescaled by
 //               alpha = exp2((m_old - m_new) log2(e) / sqrt(d)); otherwise the stale max
 //               is kept (P entries stay <= 256, and O and the sum use the same max, so
-//               the final quotient is unchanged). P = exp2(s log2(e)/sqrt(d) - m ...) as
-//               bf16 into 128-byte-swizzled shared memory (the A operand of PV). After
-//               the last tile O / l is read from TMEM and stored.
+//               the final quotient is unchanged). P = exp2(s log2(e)/sqrt(d) - m ...) is
+//               packed to bf16 and stored over the first 64 columns of S_g, where the next
+//               PV reads it. After the last tile O / l is read from TMEM and stored.
 // Key tiles above the diagonal are skipped; the diagonal tile is masked.
 #include <type_traits>
 
@@ -44,8 +44,40 @@ namespace mptp {
 
 constexpr int ATT_BQ = 128;   // queries per tile (two tiles per CTA)
 constexpr int ATT_BKV = 128;  // keys per tile
-constexpr int ATT_THREADS = 320;
+constexpr int ATT_THREADS = 384;  // warpgroup 0: TMA, MMA, two idle warps; 1, 2: softmax
+constexpr int ATT_REGS_CTRL = 64;    // registers per thread in warpgroup 0
+constexpr int ATT_REGS_SOFTMAX = 216;  // in the softmax warpgroups: 128 x 64 + 256 x 216 <= 384 x 168
 constexpr float ATT_RESCALE_LOG2 = 8.0f;  // lazy rescale threshold on the max, exp2 domain
+
+#ifndef MPTP_ATT_POLY8
+#define MPTP_ATT_POLY8 0
+#endif
+// Of every eight column pairs, the first ATT_POLY8 take exp2 from the polynomial below (FMA
+// pipe) and the rest from the hardware approximation (ex2.approx), to balance the two units.
+constexpr int ATT_POLY8 = MPTP_ATT_POLY8;
+
+// 2^x by range reduction and a polynomial: x = j + f with j = round(x) (added to the
+// exponent field) and f in [-1/2, 1/2]; 2^f from the degree-3 polynomial minimising the
+// maximum relative error on that interval (Remez exchange; max relative error 7.5e-5,
+// below the bf16 rounding of P). x is clamped at -125 so that the result stays normal.
+constexpr float ATT_EXP2_C0 = 0.99992807f;
+constexpr float ATT_EXP2_C1 = 0.69326099f;
+constexpr float ATT_EXP2_C2 = 0.24261112f;
+constexpr float ATT_EXP2_C3 = 0.055171669f;
+constexpr float ATT_ROUND_MAGIC = 12582912.0f;  // 1.5 * 2^23: x + magic rounds x to an integer
+
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+    x.x = fmaxf(x.x, -125.0f);
+    x.y = fmaxf(x.y, -125.0f);
+    const float2 t = add2(x, make_float2(ATT_ROUND_MAGIC, ATT_ROUND_MAGIC));  // j in the low mantissa bits
+    const float2 j = add2(t, make_float2(-ATT_ROUND_MAGIC, -ATT_ROUND_MAGIC));
+    const float2 f = fma2(j, make_float2(-1.0f, -1.0f), x);  // exact
+    float2 p = fma2(make_float2(ATT_EXP2_C3, ATT_EXP2_C3), f, make_float2(ATT_EXP2_C2, ATT_EXP2_C2));
+    p = fma2(p, f, make_float2(ATT_EXP2_C1, ATT_EXP2_C1));
+    p = fma2(p, f, make_float2(ATT_EXP2_C0, ATT_EXP2_C0));
+    return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
+                       __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
+}
 
 template <int D>
 struct AttnCfg {
@@ -54,15 +86,15 @@ struct AttnCfg {
     static constexpr int BOX_BYTES = 128 * 64;            // 128 rows x 32 bf16
     static constexpr int Q_BYTES = NB * BOX_BYTES;        // one query tile
     static constexpr int KV_TILE_BYTES = NB * BOX_BYTES;  // one K or one V tile
-    static constexpr int KST = D == 64 ? 3 : 2;           // K ring stages
-    static constexpr int VST = D == 64 ? 3 : 2;           // V ring stages
-    static constexpr int P_BYTES = ATT_BQ * ATT_BKV * 2;  // two 64-key blocks, 128-byte swizzle
-    // q_full, K ring, V ring, s_full/s_empty/p_full/p_empty per query tile, drain
-    static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 2 * 4 + 1;
-    static constexpr size_t SMEM_BYTES =
-        1024 + 2 * Q_BYTES + (KST + VST) * KV_TILE_BYTES + 2 * P_BYTES + 8 * NUM_BARS + 16;
+    static constexpr int KST = D == 64 ? 4 : 3;           // K ring stages
+    static constexpr int VST = D == 64 ? 4 : 3;           // V ring stages
+    // q_full, K ring, V ring, s_full/p_full/o_full per query tile, drain
+    static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 2 * 3 + 1;
+    static constexpr size_t SMEM_BYTES = 1024 + 2 * Q_BYTES + (KST + VST) * KV_TILE_BYTES + 8 * NUM_BARS + 16;
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory per block");
-    static constexpr uint32_t TMEM_COLS = 512;  // S_A, S_B: 128 columns each; O_A, O_B: D of 128 each
+    // S_A, S_B: 128 columns each (P_g, bf16, overwrites the first 64 columns of S_g);
+    // O_A, O_B: D columns at 256 and 384.
+    static constexpr uint32_t TMEM_COLS = 512;
 };
 
 struct AttnArgs {
@@ -85,18 +117,16 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     uint8_t* sQ = smem;                                    // tile g at g * Q_BYTES
     uint8_t* sK = sQ + 2 * Cfg::Q_BYTES;                   // K stage st at st * KV_TILE_BYTES
     uint8_t* sV = sK + KST * Cfg::KV_TILE_BYTES;           // V stage st at st * KV_TILE_BYTES
-    uint8_t* sP = sV + VST * Cfg::KV_TILE_BYTES;           // P of tile g at g * P_BYTES
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * Cfg::P_BYTES);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VST * Cfg::KV_TILE_BYTES);
     uint64_t* q_full = bars;
     uint64_t* k_full = bars + 1;
     uint64_t* k_empty = k_full + KST;
     uint64_t* v_full = k_empty + KST;
     uint64_t* v_empty = v_full + VST;
-    uint64_t* s_full = v_empty + VST;   // [2]: S_g computed
-    uint64_t* s_empty = s_full + 2;     // [2]: S_g read by its softmax group
-    uint64_t* p_full = s_empty + 2;     // [2]: P_g written (and O_g rescaled)
-    uint64_t* p_empty = p_full + 2;     // [2]: PV_g done (P_g free, O_g updated)
-    uint64_t* drain_bar = p_empty + 2;
+    uint64_t* s_full = v_empty + VST;   // [2]: S_g computed (and every earlier product of tile g)
+    uint64_t* p_full = s_full + 2;      // [2]: P_g written to TMEM (and O_g rescaled)
+    uint64_t* o_full = p_full + 2;      // [2]: the last PV_g done
+    uint64_t* drain_bar = o_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::NUM_BARS);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
@@ -129,9 +159,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         }
         for (int g = 0; g < 2; ++g) {
             mbar_init(&s_full[g], 1);
-            mbar_init(&s_empty[g], 4);
             mbar_init(&p_full[g], 4);
-            mbar_init(&p_empty[g], 1);
+            mbar_init(&o_full[g], 1);
         }
         *abort_flag = 0u;
         fence_mbarrier_init();
@@ -150,95 +179,121 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const uint32_t tmem_base = *tmem_slot;
     const Ctl ctl{args.status, abort_flag, args.budget_ns};
 
-    if (warp == 0) {
-        if (lane == 0) {
-            // ---------------- TMA producer ----------------
-            mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * Cfg::Q_BYTES);
-            for (int c = 0; c < NB; ++c)
-                tma_load_2d(sQ + c * Cfg::BOX_BYTES, &tmQKV, q_full, head * D + c * 32, row_base + qt_a * ATT_BQ);
-            if (has_b)
+    if (warp < 4) {
+        reg_dealloc<ATT_REGS_CTRL>();
+        if (warp == 0) {
+            if (lane == 0) {
+                // ---------------- TMA producer ----------------
+                mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * Cfg::Q_BYTES);
                 for (int c = 0; c < NB; ++c)
-                    tma_load_2d(sQ + Cfg::Q_BYTES + c * Cfg::BOX_BYTES, &tmQKV, q_full, head * D + c * 32,
-                                row_base + qt_b * ATT_BQ);
-            // Tile j of K (column block 1 of QKV) or V (block 2) into a ring stage.
-            auto load = [&](int j, int which, uint64_t* full, uint64_t* empty, uint8_t* ring, int stages) -> bool {
-                const int st = j % stages;
-                if (!wait_bounded(&empty[st], ((j / stages) & 1) ^ 1u, ctl)) return false;
-                mbar_arrive_expect_tx(&full[st], Cfg::KV_TILE_BYTES);
-                uint8_t* dst = ring + st * Cfg::KV_TILE_BYTES;
-                for (int c = 0; c < NB; ++c)
-                    tma_load_2d(dst + c * Cfg::BOX_BYTES, &tmQKV, &full[st], which * h + head * D + c * 32,
-                                row_base + j * ATT_BKV);
-                return true;
-            };
-            constexpr int LEAD = KST - 1;  // K tiles loaded ahead of the V tile of the same index
-            bool ok = true;
-            for (int j = 0; j < LEAD && j < n && ok; ++j) ok = load(j, 1, k_full, k_empty, sK, KST);
-            for (int j = 0; j < n && ok; ++j) {
-                if (j + LEAD < n) ok = load(j + LEAD, 1, k_full, k_empty, sK, KST);
-                if (ok) ok = load(j, 2, v_full, v_empty, sV, VST);
+                    tma_load_2d(sQ + c * Cfg::BOX_BYTES, &tmQKV, q_full, head * D + c * 32, row_base + qt_a * ATT_BQ);
+                if (has_b)
+                    for (int c = 0; c < NB; ++c)
+                        tma_load_2d(sQ + Cfg::Q_BYTES + c * Cfg::BOX_BYTES, &tmQKV, q_full, head * D + c * 32,
+                                    row_base + qt_b * ATT_BQ);
+                // Tile j of K (column block 1 of QKV) or V (block 2) into a ring stage.
+                auto load = [&](int j, int which, uint64_t* full, uint64_t* empty, uint8_t* ring, int stages) -> bool {
+                    const int st = j % stages;
+                    if (!wait_bounded(&empty[st], ((j / stages) & 1) ^ 1u, ctl)) return false;
+                    mbar_arrive_expect_tx(&full[st], Cfg::KV_TILE_BYTES);
+                    uint8_t* dst = ring + st * Cfg::KV_TILE_BYTES;
+                    for (int c = 0; c < NB; ++c)
+                        tma_load_2d(dst + c * Cfg::BOX_BYTES, &tmQKV, &full[st], which * h + head * D + c * 32,
+                                    row_base + j * ATT_BKV);
+                    return true;
+                };
+                constexpr int LEAD = KST - 1;  // K tiles loaded ahead of the V tile of the same index
+                bool ok = true;
+                for (int j = 0; j < LEAD && j < n && ok; ++j) ok = load(j, 1, k_full, k_empty, sK, KST);
+                for (int j = 0; j < n && ok; ++j) {
+                    if (j + LEAD < n) ok = load(j + LEAD, 1, k_full, k_empty, sK, KST);
+                    if (ok) ok = load(j, 2, v_full, v_empty, sV, VST);
+                }
             }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
+        } else if (warp == 1) {
             // ---------------- MMA issuer ----------------
+            // The whole warp runs this loop (operands stay warp-uniform); one elected lane issues
+            // each product and commit.
+            // Per key tile j and query tile g: PV_g(j) reads P_g from TMEM, then S_g(j+1)
+            // overwrites the same columns. Products issued by one thread run in issue order,
+            // so S_g(j+1) cannot overtake the read of P_g(j); the commit after S_g(j+1) also
+            // covers PV_g(j), so s_full tells the softmax group that O_g is current.
             constexpr uint32_t IDESC_S = make_idesc_bf16(ATT_BQ, ATT_BKV, false, false);
             constexpr uint32_t IDESC_PV = make_idesc_bf16(ATT_BQ, D, false, true);
-            bool ok = wait_bounded(q_full, 0, ctl);
-            // Scores of both query tiles for key tile j (those whose causal range has it).
-            auto s_step = [&](int j) -> bool {
-                const int ks = j % KST;
-                if (!wait_bounded(&k_full[ks], (j / KST) & 1, ctl)) return false;
-                const uint32_t k0 = smem_u32(sK + ks * Cfg::KV_TILE_BYTES);
-                for (int g = 0; g < 2; ++g) {
-                    if (j >= (g ? n_b : n_a)) continue;
-                    if (j >= 1 && !wait_bounded(&s_empty[g], (j - 1) & 1, ctl)) return false;
-                    tc_fence_after();
-                    const uint32_t q0 = smem_u32(sQ + g * Cfg::Q_BYTES);
-#pragma unroll
-                    for (int k = 0; k < D / 16; ++k) {
-                        const uint32_t off = (k >> 1) * Cfg::BOX_BYTES + (k & 1) * 32;
-                        umma_bf16(tmem_base + g * 128, make_sdesc_sw64(q0 + off, 16, 512),
-                                  make_sdesc_sw64(k0 + off, 16, 512), IDESC_S, k > 0 ? 1u : 0u);
-                    }
-                    umma_commit(&s_full[g]);
-                }
-                umma_commit(&k_empty[ks]);  // K tile free once both score products are done
-                return true;
+            auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+                const bool got = wait_bounded(bar, parity, ctl);
+                return __all_sync(0xffffffffu, got) != 0;
             };
-            // O_g += P_g V_j for both query tiles.
-            auto pv_step = [&](int j) -> bool {
-                const int vs = j % VST;
-                if (!wait_bounded(&v_full[vs], (j / VST) & 1, ctl)) return false;
-                const uint32_t v0 = smem_u32(sV + vs * Cfg::KV_TILE_BYTES);
-                for (int g = 0; g < 2; ++g) {
-                    if (j >= (g ? n_b : n_a)) continue;
-                    if (!wait_bounded(&p_full[g], j & 1, ctl)) return false;
-                    tc_fence_after();
-                    const uint32_t p0 = smem_u32(sP + g * Cfg::P_BYTES);
-#pragma unroll
-                    for (int k = 0; k < ATT_BKV / 16; ++k) {
-                        const uint64_t ad = make_sdesc_sw128(p0 + (k >> 2) * (ATT_BQ * 128) + (k & 3) * 32, 16, 1024);
-                        const uint64_t bd = make_sdesc_sw64(v0 + k * 1024, Cfg::BOX_BYTES, 512);
-                        umma_bf16(tmem_base + 256 + g * 128, ad, bd, IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
-                    }
-                    umma_commit(&p_empty[g]);
+            // Descriptors are computed once; an operand at byte offset o from a base is that
+            // base's descriptor advanced by o >> 4 in its address field.
+            const uint64_t q_desc = make_sdesc_sw64(smem_u32(sQ), 16, 512);
+            const uint64_t k_desc = make_sdesc_sw64(smem_u32(sK), 16, 512);
+            const uint64_t v_desc = make_sdesc_sw64(smem_u32(sV), Cfg::BOX_BYTES, 512);
+            auto s_mma = [&](int g, int j) {
+                const uint64_t qd = q_desc + static_cast<uint32_t>((g * Cfg::Q_BYTES) >> 4);
+                const uint64_t kd = k_desc + static_cast<uint32_t>(((j % KST) * Cfg::KV_TILE_BYTES) >> 4);
+                const uint32_t d_tmem = tmem_base + g * 128;
+    #pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = ((k >> 1) * Cfg::BOX_BYTES + (k & 1) * 32) >> 4;
+                    umma_bf16_elect(d_tmem, qd + off, kd + off, IDESC_S, k > 0 ? 1u : 0u);
                 }
-                umma_commit(&v_empty[vs]);  // V tile free
-                return true;
+                umma_commit_elect(&s_full[g]);
             };
-            if (ok) ok = s_step(0);
+            auto pv_mma = [&](int g, int j) {
+                const uint64_t vd = v_desc + static_cast<uint32_t>(((j % VST) * Cfg::KV_TILE_BYTES) >> 4);
+                const uint32_t d_tmem = tmem_base + 256 + g * 128;
+                const uint32_t a_tmem = tmem_base + g * 128;
+                const uint32_t acc0 = j > 0 ? 1u : 0u;
+    #pragma unroll
+                for (int k = 0; k < ATT_BKV / 16; ++k)
+                    umma_bf16_ts_elect(d_tmem, a_tmem + k * 8, vd + ((k * 1024) >> 4), IDESC_PV, k > 0 ? 1u : acc0);
+            };
+            bool ok = wait_all(q_full, 0) && wait_all(&k_full[0], 0);
+            if (ok) {
+                tc_fence_after();
+                s_mma(0, 0);
+                if (has_b) s_mma(1, 0);
+                umma_commit_elect(&k_empty[0]);
+            }
             for (int j = 0; j < n && ok; ++j) {
-                if (j + 1 < n) ok = s_step(j + 1);
-                if (ok) ok = pv_step(j);
+                ok = wait_all(&v_full[j % VST], (j / VST) & 1);
+                bool k_next = false;  // K tile j + 1 waited for
+                for (int g = 0; g < 2 && ok; ++g) {
+                    const int ng = g ? n_b : n_a;
+                    if (j >= ng) continue;
+                    if (!wait_all(&p_full[g], j & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    pv_mma(g, j);
+                    if (j + 1 < ng) {
+                        if (!k_next) {
+                            if (!wait_all(&k_full[(j + 1) % KST], ((j + 1) / KST) & 1)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            k_next = true;
+                        }
+                        s_mma(g, j + 1);
+                    } else {
+                        umma_commit_elect(&o_full[g]);
+                    }
+                }
+                if (!ok) break;
+                umma_commit_elect(&v_empty[j % VST]);                  // V tile free once both PVs are done
+                if (k_next) umma_commit_elect(&k_empty[(j + 1) % KST]);  // K tile free after both S
             }
             // Every MMA must finish before TMEM is freed.
-            umma_commit(drain_bar);
+            umma_commit_elect(drain_bar);
             wait_drain(drain_bar, 0, args.status);
         }
     } else {
-        // ---------------- softmax (warps 2..5: tile A, 6..9: tile B) ----------------
-        const int g = (warp - 2) >> 2;
+        reg_alloc<ATT_REGS_SOFTMAX>();
+        // ---------------- softmax (warps 4..7: tile A, 8..11: tile B) ----------------
+        const int g = (warp - 4) >> 2;
         const int q = warp & 3;                         // TMEM lane quarter
         const int qrow = q * 32 + lane;                 // query row within the tile
         const int qt = g ? qt_b : qt_a;
@@ -251,50 +306,42 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         bool ok = true;
 
         // Every lane polls (one warp instruction either way, and no divergent branch).
-        auto wait_lane0 = [&](uint64_t* bar, uint32_t parity) -> bool {
+        auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
             const bool got = wait_bounded(bar, parity, ctl);
             return __all_sync(0xffffffffu, got) != 0;
         };
-        uint8_t* prow = sP + g * Cfg::P_BYTES + qrow * 128;
-        const int sw = qrow & 7;
         for (int j = 0; j < ng && ok; ++j) {
-            if (!wait_lane0(&s_full[g], j & 1)) {
+            if (!wait_all(&s_full[g], j & 1)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            uint32_t r[4][32];  // the score row, 128 columns
+            uint32_t r[4][32];  // the score row, 128 columns; then P packed in r[0], r[1]
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld32(s_addr + c * 32, r[c]);
             tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 4; ++c) reg_fence32(r[c]);
-            // The scores are in registers: the TMEM buffer may take the next tile's.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[g]);
             // Key columns at or left of the diagonal: all 128 off the diagonal tile (the
             // common case, warp-uniform, compiled without masking).
             const bool diag = (j == qt);
             const int lim = qrow + 1;
-            float m8[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) m8[k] = -INFINITY;
+            auto sv = [&](int e) { return __uint_as_float(r[e >> 5][e & 31]); };
+            float m4[4];
             auto row_max = [&](auto masked) {
+                auto v = [&](int e) { return (!decltype(masked)::value || e < lim) ? sv(e) : -INFINITY; };
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int k = 0; k < 4; ++k) m4[k] = max3f(v(2 * k), v(2 * k + 1), -INFINITY);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float v = __uint_as_float(r[c][i]);
-                        m8[i & 7] = fmaxf(m8[i & 7], (!decltype(masked)::value || 32 * c + i < lim) ? v : -INFINITY);
-                    }
+                for (int e = 8; e < ATT_BKV; e += 8)
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) m4[k] = max3f(m4[k], v(e + 2 * k), v(e + 2 * k + 1));
             };
             if (diag)
                 row_max(std::true_type{});
             else
                 row_max(std::false_type{});
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            const float mx = fmaxf(max3f(m4[0], m4[1], m4[2]), m4[3]);
             bool rescale = false;
             float alpha = 1.0f;
             if (j == 0) {
@@ -305,45 +352,43 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 l *= alpha;
                 rescale = true;
             }
-            // PV of the previous tile has read P_g and added to O_g.
-            if (j >= 1 && !wait_lane0(&p_empty[g], (j - 1) & 1)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            // P = exp2(s c2 - m c2) as bf16, 16-byte chunks: column block c >> 3 of 64 keys,
-            // chunk u = c & 7 of the row (128-byte swizzle: chunk u ^ (row & 7)).
-            const float mb = m * c2;
-            float s8[8];
+            // P = exp2(s c2 - m c2); column pair k (keys 2k, 2k+1) packed as bf16x2 into word k
+            // of r (word k <= 2k has been read by then).
+            const float2 c2v = make_float2(c2, c2);
+            const float2 nmb = make_float2(-m * c2, -m * c2);
+            float2 s4[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) s8[k] = 0.0f;
-            auto exp_store = [&](auto masked) {
+            for (int k = 0; k < 4; ++k) s4[k] = make_float2(0.0f, 0.0f);
+            auto exp_pack = [&](auto masked) {
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    uint32_t pk[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int e = 8 * c + 2 * i;  // key column
-                        float p0 = ex2_approx(fmaf(__uint_as_float(r[e >> 5][e & 31]), c2, -mb));
-                        float p1 = ex2_approx(fmaf(__uint_as_float(r[(e + 1) >> 5][(e + 1) & 31]), c2, -mb));
-                        if (decltype(masked)::value) {
-                            p0 = e < lim ? p0 : 0.0f;
-                            p1 = e + 1 < lim ? p1 : 0.0f;
-                        }
-                        s8[(2 * i) & 7] += p0;
-                        s8[(2 * i + 1) & 7] += p1;
-                        pk[i] = pack_bf16x2(p0, p1);
+                for (int k = 0; k < ATT_BKV / 2; ++k) {
+                    const float2 x = fma2(make_float2(sv(2 * k), sv(2 * k + 1)), c2v, nmb);
+                    float2 p;
+                    if ((k & 7) < ATT_POLY8) {
+                        p = exp2_poly2(x);
+                    } else {
+                        p.x = ex2_approx(x.x);
+                        p.y = ex2_approx(x.y);
                     }
-                    *reinterpret_cast<uint4*>(prow + (c >> 3) * (ATT_BQ * 128) + (((c & 7) ^ sw) << 4)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    if (decltype(masked)::value) {
+                        p.x = 2 * k < lim ? p.x : 0.0f;
+                        p.y = 2 * k + 1 < lim ? p.y : 0.0f;
+                    }
+                    s4[k & 3] = add2(s4[k & 3], p);
+                    r[k >> 5][k & 31] = pack_bf16x2(p.x, p.y);
                 }
             };
             if (diag)
-                exp_store(std::true_type{});
+                exp_pack(std::true_type{});
             else
-                exp_store(std::false_type{});
-            l += ((s8[0] + s8[1]) + (s8[2] + s8[3])) + ((s8[4] + s8[5]) + (s8[6] + s8[7]));
-            // Rows whose max rose: O_g *= alpha in TMEM before the next PV adds to it.
+                exp_pack(std::false_type{});
+            const float2 s2 = add2(add2(s4[0], s4[1]), add2(s4[2], s4[3]));
+            l += s2.x + s2.y;
+            // P_g into the first 64 columns of S_g (the A operand of PV).
+            tmem_st32(s_addr, r[0]);
+            tmem_st32(s_addr + 32, r[1]);
+            // Rows whose max rose: O_g *= alpha in TMEM before the next PV adds to it (the
+            // last PV_g is complete: s_full covered it).
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
                 for (int c = 0; c < NB; ++c) {
@@ -355,15 +400,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
                     tmem_st32(o_addr + c * 32, o);
                 }
-                tmem_wait_st();
             }
-            fence_proxy_async_smem();  // P is read by the tensor core (async proxy)
+            tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[g]);
         }
         // O / l after the last PV.
-        if (ok && ng > 0 && wait_lane0(&p_empty[g], (ng - 1) & 1)) {
+        if (ok && ng > 0 && wait_all(&o_full[g], 0)) {
             tc_fence_after();
             const float inv = 1.0f / l;
             uint4* dst = reinterpret_cast<uint4*>(args.O + static_cast<long long>(row_base + qt * ATT_BQ + qrow) * h +
