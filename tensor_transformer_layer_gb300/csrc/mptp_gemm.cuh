@@ -388,8 +388,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
             }
         }
     } else if (warp == 1) {
-        if (lane == 0 && leader) {
+        if (leader) {
             // ---------------- MMA issuer (leader CTA) ----------------
+            // The whole warp runs the issue loop, so that the operands stay warp-uniform; one
+            // elected lane issues each product and commit. Waits are polled by every lane.
+            auto wait_all = [&](uint64_t* bar, uint32_t parity) -> bool {
+                const bool got = mbar_test_wait(bar, parity) || wait_bounded(bar, parity, ctl);
+                return __all_sync(0xffffffffu, got) != 0;
+            };
             int stage = 0;
             uint32_t phase = 0;
             uint32_t tcount = 0;
@@ -408,7 +414,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                 for (int nt = 0; nt < args.tiles_per_unit && ok; ++nt, ++tcount) {
                     const uint32_t buf = tcount & 1u;
                     const uint32_t tph = (tcount >> 1) & 1u;
-                    if (!wait_bounded(&tempty_bar[buf], tph ^ 1u, ctl)) {
+                    if (!wait_all(&tempty_bar[buf], tph ^ 1u)) {
                         ok = false;
                         break;
                     }
@@ -418,29 +424,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                     // tensor cycles, and everything else it does per stage must fit beside them.
                     // Stage descriptors are the stage-0 ones advanced in their address field.
                     for (int kb = p.kb_begin; kb < p.kb_end; ++kb) {
-                        if (!mbar_test_wait(&full_bar[stage], phase) && !wait_bounded(&full_bar[stage], phase, ctl)) {
+                        if (!wait_all(&full_bar[stage], phase)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint64_t ad0 = ad_base + static_cast<uint64_t>(stage) * (Cfg::A_BYTES >> 4);
                         const uint64_t bd0 = bd_base + static_cast<uint64_t>(stage) * (Cfg::B_BYTES >> 4);
-                        umma_bf16_pair(d_tmem, ad0, bd0, idesc, kb > p.kb_begin ? 1u : 0u);
+                        umma_bf16_pair_elect(d_tmem, ad0, bd0, idesc, kb > p.kb_begin ? 1u : 0u);
 #pragma unroll
                         for (int k = 1; k < BK / UMMA_K; ++k)
-                            umma_bf16_pair_acc(d_tmem, ad0 + k * a_kstep, bd0 + k * b_kstep, idesc);
-                        umma_commit_pair_multicast(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
+                            umma_bf16_pair_acc_elect(d_tmem, ad0 + k * a_kstep, bd0 + k * b_kstep, idesc);
+                        umma_commit_pair_multicast_elect(&empty_bar[stage], 0x3);  // frees the stage in both CTAs
                         if (++stage == STAGES) {
                             stage = 0;
                             phase ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    umma_commit_pair_multicast(&tfull_bar[buf], 0x3);  // accumulators ready in both CTAs
+                    umma_commit_pair_multicast_elect(&tfull_bar[buf], 0x3);  // accumulators ready in both CTAs
                 }
             }
             // Every MMA of the pair must finish before either CTA frees TMEM or exits.
-            umma_commit_pair(drain_bar);
+            umma_commit_pair_elect(drain_bar);
             wait_drain(drain_bar, 0, args.status);
         }
     } else {
