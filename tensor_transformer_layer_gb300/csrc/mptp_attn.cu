@@ -483,7 +483,8 @@ extern "C" mp_status mp_attn_fwd(const mp_bf16* X, const mp_bf16* Wqkv, const mp
 
     // QKV = X Wqkv: all shards' heads in one column-parallel launch (Wqkv MN-major).
     TmapSet m1{};
-    if (!make_tmap_bf16(&m1.a, X, h, T, h, 64, BM) || !make_tmap_bf16(&m1.b, Wqkv, 3 * h, h, 3 * h, 64, 64) ||
+    int b1f = 0;
+    if (!make_tmap_bf16(&m1.a, X, h, T, h, 64, BM) || !(b1f = make_tmap_mn_operand(&m1.b, Wqkv, 3 * h, h, 3 * h)) ||
         !make_tmap_bf16_out(&m1.o0, QKV, 3 * h, T, 3 * h))
         return MP_ERR_CUDA;
     GemmArgs a1{};
@@ -493,7 +494,7 @@ extern "C" mp_status mp_attn_fwd(const mp_bf16* X, const mp_bf16* Wqkv, const mp
     a1.pr.num_units = a1.pr.num_m_blocks * ceil_div(3 * h, 256);
     a1.pr.n_fastest = n_fastest_order(Tb * h, hb * 3 * h);
     a1.pr.kb_end = h / BK;
-    a1.pr.b_mn = 1;
+    a1.pr.b_mn = b1f;
     a1.tiles_per_unit = 1;
     a1.status = d_status;
     a1.budget_ns = budget;
@@ -519,7 +520,8 @@ extern "C" mp_status mp_attn_fwd(const mp_bf16* X, const mp_bf16* Wqkv, const mp
     // out = sum_i O_i Wo_i: the K-loop runs over the heads' columns in ascending order, i.e.
     // shard 0's heads, then shard 1's, ... (the g sum; a K block may span two shards).
     TmapSet m3{};
-    if (!make_tmap_bf16(&m3.a, O, h, T, h, 64, BM) || !make_tmap_bf16(&m3.b, Wo, h, h, h, 64, 64) ||
+    int b3f = 0;
+    if (!make_tmap_bf16(&m3.a, O, h, T, h, 64, BM) || !(b3f = make_tmap_mn_operand(&m3.b, Wo, h, h, h)) ||
         !make_tmap_bf16_out(&m3.o0, out, h, T, h))
         return MP_ERR_CUDA;
     GemmArgs a3{};
@@ -530,7 +532,7 @@ extern "C" mp_status mp_attn_fwd(const mp_bf16* X, const mp_bf16* Wqkv, const mp
     a3.pr.n_fastest = n_fastest_order(Tb * h, hb * h);
     a3.pr.kb_begin = 0;
     a3.pr.kb_end = h / BK;
-    a3.pr.b_mn = 1;
+    a3.pr.b_mn = b3f;
     a3.tiles_per_unit = 1;
     a3.status = d_status;
     a3.budget_ns = budget;

@@ -144,7 +144,8 @@ extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const i
 
         // K11: dE_i = dZ_i^T X (M = vs, N = h, K = T; both operands MN-major).
         TmapSet m11{};
-        if (!make_tmap_bf16(&m11.a, dz, vs, T, vs, 64, 64) || !make_tmap_bf16(&m11.b, X, h, T, h, 64, 64) ||
+        int a11f = 0, b11f = 0;
+        if (!(a11f = make_tmap_mn_operand(&m11.a, dz, vs, T, vs)) || !(b11f = make_tmap_mn_operand(&m11.b, X, h, T, h)) ||
             !make_tmap_bf16_out(&m11.o0, dEi, h, vs, h))
             return MP_ERR_CUDA;
         GemmArgs a11{};
@@ -155,8 +156,8 @@ extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const i
         a11.pr.n_fastest = n_fastest_order(Tb * vs, Tb * h);
         a11.pr.kb_begin = 0;
         a11.pr.kb_end = ceil_div(T, BK);
-        a11.pr.a_mn = 1;
-        a11.pr.b_mn = 1;
+        a11.pr.a_mn = a11f;
+        a11.pr.b_mn = b11f;
         a11.tiles_per_unit = 1;
         a11.status = d_status;
         a11.budget_ns = budget;
@@ -164,7 +165,8 @@ extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const i
 
         // K12: dX (+)= dZ_i E_i (M = T, N = h, K = vs; A K-major, B = E_i MN-major), shards in order.
         TmapSet m12{};
-        if (!make_tmap_bf16(&m12.a, dz, vs, T, vs, 64, BM) || !make_tmap_bf16(&m12.b, Ei, h, vs, h, 64, 64) ||
+        int b12f = 0;
+        if (!make_tmap_bf16(&m12.a, dz, vs, T, vs, 64, BM) || !(b12f = make_tmap_mn_operand(&m12.b, Ei, h, vs, h)) ||
             !make_tmap_bf16_out(&m12.o0, dX, h, T, h))
             return MP_ERR_CUDA;
         GemmArgs a12{};
@@ -176,7 +178,7 @@ extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const i
         a12.pr.kb_begin = 0;
         a12.pr.kb_end = vs / BK;
         a12.pr.a_mn = 0;
-        a12.pr.b_mn = 1;
+        a12.pr.b_mn = b12f;
         a12.tiles_per_unit = 1;
         a12.acc = acc;
         a12.ld_acc = h;

@@ -48,6 +48,27 @@ bool make_tmap_bf16_sw64(CUtensorMap* map, const void* base, uint64_t inner, uin
     return make_tmap_bf16_sw(map, base, inner, outer, pitch_elems, box_inner, box_outer, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+bool make_tmap_bf16_mn3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
+                         uint32_t blocks) {
+    auto fn = encode_fn();
+    if (fn == nullptr || inner % 64 != 0) return false;
+    // (column within a 64-wide block, row, block): a box of 64 rows x `blocks` blocks lands as
+    // `blocks` consecutive 64-row x 128-byte slabs, the layout of as many 2-D boxes.
+    cuuint64_t dims[3] = {64, outer, inner / 64};
+    cuuint64_t strides[2] = {pitch_elems * 2, 128};
+    cuuint32_t box[3] = {64, 64, blocks};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int make_tmap_mn_operand(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems) {
+    if (inner % 64 == 0) return make_tmap_bf16_mn3d(map, base, inner, outer, pitch_elems, 2) ? 2 : 0;
+    return make_tmap_bf16(map, base, inner, outer, pitch_elems, 64, 64) ? 1 : 0;
+}
+
 bool make_tmap_bf16_out(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems) {
     return make_tmap_bf16_sw(map, base, inner, outer, pitch_elems, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }

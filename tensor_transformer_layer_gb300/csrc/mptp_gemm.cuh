@@ -94,7 +94,8 @@ struct ProbInfo {
     int num_units;            // num_m_blocks * unit columns
     int n_fastest;            // unit order: 0 = row blocks fastest, 1 = column units fastest
     int kb_begin, kb_end;     // K blocks (of BK) to accumulate, ascending
-    int a_mn, b_mn;           // operand majorness: 1 = M (N) contiguous, 0 = K contiguous
+    int a_mn, b_mn;           // operand majorness: 0 = K contiguous; 1 = M (N) contiguous, loaded as
+                              // 64-wide 2-D boxes; 2 = the same through a 3-D map (one box per stage)
 };
 
 struct GemmArgs {
@@ -365,14 +366,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                         mbar_arrive_expect_tx_cluster(full_leader, Cfg::STAGE_BYTES);
                         uint8_t* a_dst = sA + stage * Cfg::A_BYTES;
                         uint8_t* b_dst = sB + stage * Cfg::B_BYTES;
-                        if (p.a_mn) {
+                        if (p.a_mn == 2) {  // all 64-wide M blocks of the stage in one 3-D box
+                            tma_load_3d_pair(a_dst, tmA, full_leader, 0, kb * BK, arow / 64);
+                        } else if (p.a_mn) {
 #pragma unroll
                             for (int j = 0; j < BM / 64; ++j)
                                 tma_load_2d_pair(a_dst + j * 8192, tmA, full_leader, arow + j * 64, kb * BK);
                         } else {
                             tma_load_2d_pair(a_dst, tmA, full_leader, kb * BK, arow);
                         }
-                        if (p.b_mn) {
+                        if (p.b_mn == 2) {
+                            tma_load_3d_pair(b_dst, tmB, full_leader, 0, kb * BK, bcol / 64);
+                        } else if (p.b_mn) {
 #pragma unroll
                             for (int j = 0; j < BNH / 64; ++j)
                                 tma_load_2d_pair(b_dst + j * 8192, tmB, full_leader, bcol + j * 64, kb * BK);
@@ -747,6 +752,7 @@ inline cudaError_t launch_gemm_tc(const TmapSet& maps, const GemmArgs& args, int
     using Cfg = GemmCfg<BN, EPI, NE>;
     auto kern = gemm_tc_kernel<BN, EPI, NE>;
     if (BN % 128 != 0 && args.pr.b_mn) return cudaErrorInvalidValue;  // MN-major B needs 64-column boxes per CTA
+    if (args.pr.b_mn == 2 && BN != 256) return cudaErrorInvalidValue;  // 3-D B box: two 64-column blocks per CTA
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_BYTES));
     if (e != cudaSuccess) return e;

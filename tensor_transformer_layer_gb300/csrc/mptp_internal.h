@@ -25,6 +25,14 @@ bool make_tmap_bf16_sw64(CUtensorMap* map, const void* base, uint64_t inner, uin
 
 // Tensor map for an epilogue output: 32 x 32 boxes, 64-byte swizzle (the layout
 // the epilogue stages rows in before its TMA store).
+// MN-major operand [outer rows, inner columns] as a 3-D map of 64-column blocks (SW128), box of
+// 64 rows x `blocks` blocks; inner must be a multiple of 64.
+bool make_tmap_bf16_mn3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems,
+                         uint32_t blocks);
+// MN-major GEMM operand [outer rows, inner columns] for CTA-pair tiles (two 64-wide blocks per
+// CTA and stage): a 3-D map when inner is a multiple of 64 (returns majorness flag 2: one TMA box
+// per stage), else 64-wide 2-D boxes (flag 1). 0: the map could not be encoded.
+int make_tmap_mn_operand(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems);
 bool make_tmap_bf16_out(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems);
 
 // Unit order for a GEMM whose A operand (M side) has a_bytes and B operand (N side)

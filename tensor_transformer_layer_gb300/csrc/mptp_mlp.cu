@@ -114,12 +114,14 @@ extern "C" mp_status mp_mlp_fwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
 
     // K1: column-parallel GEMM + GeLU over all shards' columns: U = X A (A MN-major), Y = GeLU(U).
     TmapSet m1{};
-    if (!make_tmap_bf16(&m1.a, X, h, T, h, 64, BM) || !make_tmap_bf16(&m1.b, A, f, h, f, 64, 64) ||
+    int b1 = 0;
+    if (!make_tmap_bf16(&m1.a, X, h, T, h, 64, BM) || !(b1 = make_tmap_mn_operand(&m1.b, A, f, h, f)) ||
         !make_tmap_bf16_out(&m1.o0, Y, f, T, f) ||
         (U_save && !make_tmap_bf16_out(&m1.o1, U_save, f, T, f)))
         return MP_ERR_CUDA;
     GemmArgs a1 = launch_args(d_status);
     a1.pr = problem(T, f, 256, 0, h / BK, false, true, Tb * h, hb * f);
+    a1.pr.b_mn = b1;
     a1.has_out1 = U_save ? 1 : 0;
     a1.out0 = reinterpret_cast<__nv_bfloat16*>(Y);
     a1.ld_out0 = f;
@@ -131,11 +133,13 @@ extern "C" mp_status mp_mlp_fwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
     // visited for i = 0..t-1 in order, all into the same accumulator (the g sum).
     const int fs = f / t;
     TmapSet m2{};
-    if (!make_tmap_bf16(&m2.a, Y, f, T, f, 64, BM) || !make_tmap_bf16(&m2.b, B, h, f, h, 64, 64) ||
+    int b2 = 0;
+    if (!make_tmap_bf16(&m2.a, Y, f, T, f, 64, BM) || !(b2 = make_tmap_mn_operand(&m2.b, B, h, f, h)) ||
         !make_tmap_bf16_out(&m2.o0, Z, h, T, h))
         return MP_ERR_CUDA;
     GemmArgs a2 = launch_args(d_status);
     a2.pr = problem(T, h, 256, 0 * (fs / BK), t * (fs / BK), false, true, Tb * f, hb * f);
+    a2.pr.b_mn = b2;
     a2.out0 = reinterpret_cast<__nv_bfloat16*>(Z);
     a2.ld_out0 = h;
     if (launch_gemm_tc<256, MPTP_STORE_EPI, 4>(m2, a2, sms, s) != cudaSuccess) return MP_ERR_CUDA;
@@ -192,21 +196,27 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
 
     // K5a: dA = X^T dU (M = h, N = f, K = T).  Both operands MN-major.
     TmapSet m5{};
-    if (!make_tmap_bf16(&m5.a, X, h, T, h, 64, 64) || !make_tmap_bf16(&m5.b, dU_ws, f, T, f, 64, 64) ||
+    int a5f = 0, b5f = 0;
+    if (!(a5f = make_tmap_mn_operand(&m5.a, X, h, T, h)) || !(b5f = make_tmap_mn_operand(&m5.b, dU_ws, f, T, f)) ||
         !make_tmap_bf16_out(&m5.o0, dA, f, h, f))
         return MP_ERR_CUDA;
     GemmArgs a5 = launch_args(d_status);
     a5.pr = problem(h, f, 256, 0, ceil_div(T, BK), true, true, Tb * h, Tb * f);
+    a5.pr.a_mn = a5f;
+    a5.pr.b_mn = b5f;
     a5.out0 = reinterpret_cast<__nv_bfloat16*>(dA);
     a5.ld_out0 = f;
 
     // K5b: dB = Y^T dZ (M = f, N = h, K = T).  Both operands MN-major.
     TmapSet m6{};
-    if (!make_tmap_bf16(&m6.a, Y, f, T, f, 64, 64) || !make_tmap_bf16(&m6.b, dZ, h, T, h, 64, 64) ||
+    int a6f = 0, b6f = 0;
+    if (!(a6f = make_tmap_mn_operand(&m6.a, Y, f, T, f)) || !(b6f = make_tmap_mn_operand(&m6.b, dZ, h, T, h)) ||
         !make_tmap_bf16_out(&m6.o0, dB, h, f, h))
         return MP_ERR_CUDA;
     GemmArgs a6 = launch_args(d_status);
     a6.pr = problem(f, h, 256, 0, ceil_div(T, BK), true, true, Tb * f, Tb * h);
+    a6.pr.a_mn = a6f;
+    a6.pr.b_mn = b6f;
     a6.out0 = reinterpret_cast<__nv_bfloat16*>(dB);
     a6.ld_out0 = h;
 
