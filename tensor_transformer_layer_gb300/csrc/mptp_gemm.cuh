@@ -215,37 +215,52 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // Functions, eq. 7.1.26 (|error of erf| <= 1.5e-7 for x >= 0):
 //   erf(x) = 1 - (a1 s + a2 s^2 + a3 s^3 + a4 s^4 + a5 s^5) e^{-x^2},  s = 1 / (1 + p x).
 // With x = |u| / sqrt 2 and q = (1 - erf(x)) / 2, Phi(u) = 1 - q for u >= 0 and q
-// for u < 0; phi(u) = e^{-x^2} / sqrt(2 pi) reuses the same exponential. In fp32
-// with the hardware ex2/rcp approximations the CDF error stays below 1e-6, far
-// under the bf16 output spacing.
-struct NormalCdfPdf {
-    float cdf, pdf;
-};
+// for u < 0; phi(u) = e^{-x^2} / sqrt(2 pi) reuses the same exponential, and
+// GeLU(u) = u Phi(u) = max(u, 0) - |u| q. In fp32 with the hardware ex2/rcp
+// approximations the CDF error stays below 1e-6, far under the bf16 output spacing.
+// Two values at a time: the arithmetic runs as packed two-lane instructions.
 __device__ __forceinline__ float rcp_approx(float x) {
     float y;
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ NormalCdfPdf normal_cdf_pdf(float u) {
-    const float x = fabsf(u) * 0.70710678118654752f;
-    const float s = rcp_approx(fmaf(0.3275911f, x, 1.0f));
-    float poly = fmaf(1.061405429f, s, -1.453152027f);
-    poly = fmaf(poly, s, 1.421413741f);
-    poly = fmaf(poly, s, -0.284496736f);
-    poly = fmaf(poly, s, 0.254829592f);
-    poly *= s;
-    const float e = ex2_approx(-(x * x) * 1.4426950408889634f);  // e^{-x^2}
-    const float q = 0.5f * poly * e;
-    return {u >= 0.0f ? 1.0f - q : q, 0.39894228040143268f * e};
+struct NormalCdfPdf2 {
+    float2 a;      // |u|
+    float2 nq;     // -q = -(1 - erf(|u| / sqrt 2)) / 2
+    float2 e;      // e^{-u^2 / 2}
+};
+__device__ __forceinline__ NormalCdfPdf2 normal_tail2(float2 u) {
+    constexpr float P_OVER_SQRT2 = 0.23164189f;   // 0.3275911 / sqrt 2
+    constexpr float NEG_HALF_LOG2E = -0.72134752f;  // e^{-u^2/2} = 2^{u^2 * this}
+    // -a_k / 2, so that the polynomial times e gives -q directly
+    constexpr float C1 = -0.127414796f, C2 = 0.142248368f, C3 = -0.7107068705f, C4 = 0.7265760135f,
+                    C5 = -0.5307027145f;
+    auto dup = [](float c) { return make_float2(c, c); };
+    NormalCdfPdf2 r;
+    r.a = make_float2(fabsf(u.x), fabsf(u.y));
+    const float2 d = fma2(r.a, dup(P_OVER_SQRT2), dup(1.0f));
+    const float2 s = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+    float2 poly = fma2(s, dup(C5), dup(C4));
+    poly = fma2(poly, s, dup(C3));
+    poly = fma2(poly, s, dup(C2));
+    poly = fma2(poly, s, dup(C1));
+    poly = mul2(poly, s);
+    const float2 w = mul2(mul2(u, u), dup(NEG_HALF_LOG2E));
+    r.e = make_float2(ex2_approx(w.x), ex2_approx(w.y));
+    r.nq = mul2(poly, r.e);
+    return r;
 }
-
-// GeLU(u) = u Phi(u) (erf form).
-__device__ __forceinline__ float gelu_f(float u) { return u * normal_cdf_pdf(u).cdf; }
-
+// GeLU(u) = max(u, 0) - |u| q.
+__device__ __forceinline__ float2 gelu2(float2 u) {
+    const NormalCdfPdf2 t = normal_tail2(u);
+    return fma2(t.a, t.nq, make_float2(fmaxf(u.x, 0.0f), fmaxf(u.y, 0.0f)));
+}
 // GeLU'(u) = Phi(u) + u phi(u).
-__device__ __forceinline__ float gelu_prime_f(float u) {
-    const NormalCdfPdf c = normal_cdf_pdf(u);
-    return fmaf(u, c.pdf, c.cdf);
+__device__ __forceinline__ float2 gelu_prime2(float2 u) {
+    constexpr float INV_SQRT_2PI = 0.39894228040143268f;
+    const NormalCdfPdf2 t = normal_tail2(u);
+    const float2 cdf = make_float2(u.x >= 0.0f ? 1.0f + t.nq.x : -t.nq.x, u.y >= 0.0f ? 1.0f + t.nq.y : -t.nq.y);
+    return fma2(u, mul2(t.e, make_float2(INV_SQRT_2PI, INV_SQRT_2PI)), cdf);
 }
 
 // One warp writes its 32 rows x 32 columns of bf16 (thread = row) into one of its
@@ -559,16 +574,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                             emit(&maps.o1, args.out1, args.ld_out1, pk);
                         }
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            pk[j] = pack_bf16x2(gelu_f(__uint_as_float(r[2 * j])), gelu_f(__uint_as_float(r[2 * j + 1])));
+                        for (int j = 0; j < 16; ++j) {
+                            const float2 g = gelu2(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])));
+                            pk[j] = pack_bf16x2(g.x, g.y);
+                        }
                         emit(tmO0, args.out0, args.ld_out0, pk);
                     } else if constexpr (epi_math(EPI) == EPI_DGELU) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
-                            const float g0 = __uint_as_float(r[2 * j]) * gelu_prime_f(bf16_lo(uw[j]));
-                            const float g1 = __uint_as_float(r[2 * j + 1]) * gelu_prime_f(bf16_hi(uw[j]));
-                            pk[j] = pack_bf16x2(g0, g1);
+                            const float2 gp = gelu_prime2(make_float2(bf16_lo(uw[j]), bf16_hi(uw[j])));
+                            const float2 g = mul2(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), gp);
+                            pk[j] = pack_bf16x2(g.x, g.y);
                         }
                         emit(tmO0, args.out0, args.ld_out0, pk);
                     } else if constexpr (EPI == EPI_DZ) {
