@@ -49,36 +49,6 @@ constexpr int ATT_REGS_CTRL = 64;    // registers per thread in warpgroup 0
 constexpr int ATT_REGS_SOFTMAX = 216;  // in the softmax warpgroups: 128 x 64 + 256 x 216 <= 384 x 168
 constexpr float ATT_RESCALE_LOG2 = 8.0f;  // lazy rescale threshold on the max, exp2 domain
 
-#ifndef MPTP_ATT_POLY8
-#define MPTP_ATT_POLY8 0
-#endif
-// Of every eight column pairs, the first ATT_POLY8 take exp2 from the polynomial below (FMA
-// pipe) and the rest from the hardware approximation (ex2.approx), to balance the two units.
-constexpr int ATT_POLY8 = MPTP_ATT_POLY8;
-
-// 2^x by range reduction and a polynomial: x = j + f with j = round(x) (added to the
-// exponent field) and f in [-1/2, 1/2]; 2^f from the degree-3 polynomial minimising the
-// maximum relative error on that interval (Remez exchange; max relative error 7.5e-5,
-// below the bf16 rounding of P). x is clamped at -125 so that the result stays normal.
-constexpr float ATT_EXP2_C0 = 0.99992807f;
-constexpr float ATT_EXP2_C1 = 0.69326099f;
-constexpr float ATT_EXP2_C2 = 0.24261112f;
-constexpr float ATT_EXP2_C3 = 0.055171669f;
-constexpr float ATT_ROUND_MAGIC = 12582912.0f;  // 1.5 * 2^23: x + magic rounds x to an integer
-
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-    x.x = fmaxf(x.x, -125.0f);
-    x.y = fmaxf(x.y, -125.0f);
-    const float2 t = add2(x, make_float2(ATT_ROUND_MAGIC, ATT_ROUND_MAGIC));  // j in the low mantissa bits
-    const float2 j = add2(t, make_float2(-ATT_ROUND_MAGIC, -ATT_ROUND_MAGIC));
-    const float2 f = fma2(j, make_float2(-1.0f, -1.0f), x);  // exact
-    float2 p = fma2(make_float2(ATT_EXP2_C3, ATT_EXP2_C3), f, make_float2(ATT_EXP2_C2, ATT_EXP2_C2));
-    p = fma2(p, f, make_float2(ATT_EXP2_C1, ATT_EXP2_C1));
-    p = fma2(p, f, make_float2(ATT_EXP2_C0, ATT_EXP2_C0));
-    return make_float2(__int_as_float(__float_as_int(p.x) + (__float_as_int(t.x) << 23)),
-                       __int_as_float(__float_as_int(p.y) + (__float_as_int(t.y) << 23)));
-}
-
 template <int D>
 struct AttnCfg {
     static_assert(D == 64 || D == 96, "head width");
@@ -363,13 +333,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 #pragma unroll
                 for (int k = 0; k < ATT_BKV / 2; ++k) {
                     const float2 x = fma2(make_float2(sv(2 * k), sv(2 * k + 1)), c2v, nmb);
-                    float2 p;
-                    if ((k & 7) < ATT_POLY8) {
-                        p = exp2_poly2(x);
-                    } else {
-                        p.x = ex2_approx(x.x);
-                        p.y = ex2_approx(x.y);
-                    }
+                    float2 p = make_float2(ex2_approx(x.x), ex2_approx(x.y));
                     if (decltype(masked)::value) {
                         p.x = 2 * k < lim ? p.x : 0.0f;
                         p.y = 2 * k + 1 < lim ? p.y : 0.0f;
