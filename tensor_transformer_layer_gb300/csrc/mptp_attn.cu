@@ -462,9 +462,7 @@ extern "C" mp_status mp_attn_fwd(const mp_bf16* X, const mp_bf16* Wqkv, const mp
     a1.tiles_per_unit = 1;
     a1.status = d_status;
     a1.budget_ns = budget;
-    a1.out0 = reinterpret_cast<__nv_bfloat16*>(QKV);
-    a1.ld_out0 = 3 * h;
-    if (launch_gemm_tc<256, EPI_STORE_G, 4>(m1, a1, sms, cs) != cudaSuccess) return MP_ERR_CUDA;
+    if (launch_gemm_tc<256, EPI_STORE, 4>(m1, a1, sms, cs) != cudaSuccess) return MP_ERR_CUDA;
 
     // Per-head causal attention.
     CUtensorMap tq;
@@ -502,8 +500,6 @@ extern "C" mp_status mp_attn_fwd(const mp_bf16* X, const mp_bf16* Wqkv, const mp
     a3.tiles_per_unit = 1;
     a3.status = d_status;
     a3.budget_ns = budget;
-    a3.out0 = reinterpret_cast<__nv_bfloat16*>(out);
-    a3.ld_out0 = h;
-    if (launch_gemm_tc<256, EPI_STORE_G, 4>(m3, a3, sms, cs) != cudaSuccess) return MP_ERR_CUDA;
+    if (launch_gemm_tc<256, EPI_STORE, 4>(m3, a3, sms, cs) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }

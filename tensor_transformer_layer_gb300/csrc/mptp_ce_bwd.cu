@@ -161,9 +161,7 @@ extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const i
         a11.tiles_per_unit = 1;
         a11.status = d_status;
         a11.budget_ns = budget;
-        a11.out0 = dEi;
-        a11.ld_out0 = h;
-        if (launch_gemm_tc<256, EPI_STORE_G, 4>(m11, a11, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+        if (launch_gemm_tc<256, EPI_STORE, 4>(m11, a11, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
         // K12: dX (+)= dZ_i E_i (M = T, N = h, K = vs; A K-major, B = E_i MN-major), shards in order.
         TmapSet m12{};

@@ -63,16 +63,18 @@ static BwdSchedule bwd_schedule() {
 // Cost of one output tile in K-block times: its K blocks plus about two for the epilogue.
 constexpr int EPI_KB = 2;
 
-// Epilogue of the plain-store GEMMs (K2, K4, K5): bf16 rows stored from registers, which
-// leaves room for a seventh pipeline stage.
+// Epilogues: bf16 rows staged in shared memory and written by TMA stores (whole lines). The
+// register-store forms (EPI_*_G: 16-byte pieces of 32 rows per store instruction, and a seventh
+// pipeline stage) finish a lone launch as fast, but 200 back-to-back steps at the power cap ran
+// 1.3% slower with them: the partial-line writes cost clock.
 #ifndef MPTP_STORE_EPI
-#define MPTP_STORE_EPI EPI_STORE_G
+#define MPTP_STORE_EPI EPI_STORE
 #endif
 #ifndef MPTP_GELU_EPI
-#define MPTP_GELU_EPI EPI_GELU_G
+#define MPTP_GELU_EPI EPI_GELU
 #endif
 #ifndef MPTP_DGELU_EPI
-#define MPTP_DGELU_EPI EPI_DGELU_G
+#define MPTP_DGELU_EPI EPI_DGELU
 #endif
 // Epilogue warps of K1 and K3.
 #ifndef MPTP_K13_NE
