@@ -8,25 +8,27 @@
 // of A and columns [BN/2 r, +BN/2) of B; the leader (r = 0) issues one
 // tcgen05.mma with M = 256 that reads both CTAs' shared memory and writes each
 // CTA's 128 x BN accumulator into that CTA's TMEM. Per SM this halves the B
-// traffic, so a stage is 32 KB (BN = 256) and the ring holds 6 stages.
+// traffic, so a stage is 32 KB (BN = 256) and the ring holds 6 or 7 stages.
 //
 // Grid = 2 x the fewest co-resident pairs that finish the units in the fewest
 // rounds; 64 + 32*NE threads per CTA:
 //   warp 0      TMA producer (one lane) in each CTA: its A and B halves per
 //               stage, completion signalled on the leader's `full` barrier.
 //   warp 1      TMEM allocator (whole warp, both CTAs) and, in the leader only,
-//               the MMA issuer (one lane): 4 x tcgen05.mma (K = 16) per stage into
-//               one of two TMEM accumulators (BN fp32 columns each per CTA); its
-//               commits arrive on the `empty` / `tmem full` barriers of both CTAs.
+//               the MMA issuer: the whole warp runs the issue loop (so descriptors
+//               and addresses stay in uniform registers) and one elected lane issues
+//               4 x tcgen05.mma (K = 16) per stage into one of two TMEM accumulators
+//               (BN fp32 columns each per CTA); its commits arrive on the `empty` /
+//               `tmem full` barriers of both CTAs.
 //   warps 2..   NE epilogue warps (4 or 8) in each CTA: tcgen05.ld 32 rows x 32
 //               columns (TMEM lane quarter = warp % 4, thread = output row; with 8
 //               warps two warps share a quarter and split the columns), fused math,
-//               then bf16 rows either stored straight from registers (plain store,
-//               which leaves room for one more pipeline stage) or staged in a
-//               64-byte-swizzled shared box per warp and written by TMA stores (32x32
-//               boxes), or cross-entropy partials. An
-//               accumulator is handed back (to the leader) as soon as its last
-//               columns are in registers, so it overlaps the next tile's MMAs.
+//               then bf16 rows staged in a 64-byte-swizzled shared box per warp and
+//               written by TMA stores (32x32 boxes), or stored straight from
+//               registers (the EPI_*_G forms, which leave room for one more
+//               pipeline stage), or cross-entropy partials. An accumulator is
+//               handed back (to the leader) as soon as its last columns are in
+//               registers, so it overlaps the next tile's MMAs.
 //
 // A work unit is one 256-row block and `tiles_per_unit` consecutive BN-wide
 // column tiles (1 for plain GEMMs; several for the cross-entropy, whose epilogue
@@ -38,6 +40,8 @@
 // Operand majorness: K-major = K contiguous in global memory (row-major [rows, K]),
 // MN-major = M (or N) contiguous (row-major [K, rows]); both are loaded by TMA
 // with the 128-byte swizzle and described to the MMA without any transpose copy.
+// An MN-major operand's stage is two 64-column blocks per CTA, loaded by one 3-D
+// box (majorness flag 2) or two 2-D boxes (flag 1).
 //
 // Every mbarrier wait is bounded by a time budget; on expiry the kernel sets
 // MP_DEV_TIMEOUT in the status word, raises a CTA-wide abort flag, lets its own
