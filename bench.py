@@ -334,13 +334,20 @@ def time_next_rows(step, reps, flush):
     dloss = torch.full((T,), 1.0 / T, dtype=torch.float32, device=d["Xc"].device)
     dXc = torch.empty(T, h, dtype=torch.bfloat16, device=d["Xc"].device)
     dE = torch.empty(v_pad, h, dtype=torch.bfloat16, device=d["Xc"].device)
-    wsb = torch.empty(mp.mp_vocab_ce_bwd_workspace_bytes(T, h, v_pad, t), dtype=torch.uint8, device=d["Xc"].device)
     mp.mp_vocab_ce(d["Xc"], d["E"], d["target"], d["loss"], step.ws, v_valid=v_valid, t=t)
-    fn = lambda: mp.mp_vocab_ce_bwd(d["Xc"], d["E"], d["target"], d["loss"], dloss, dXc, dE, wsb, v_valid=v_valid,
-                                    t=t, d_status=step.status)
-    fn()
-    ms = event_median(fn, reps, flush)
-    step.check_status()
+    # Both workspace sizes: the minimum (one shard of dZ at a time) and the one-pass size
+    # (every shard's dZ: one GEMM of each kind).
+    ce_ms = {}
+    for mode, size in (("shard_by_shard", mp.mp_vocab_ce_bwd_workspace_bytes),
+                       ("one_pass", mp.mp_vocab_ce_bwd_workspace_bytes_one_pass)):
+        wsb = torch.empty(size(T, h, v_pad, t), dtype=torch.uint8, device=d["Xc"].device)
+        fn = lambda: mp.mp_vocab_ce_bwd(d["Xc"], d["E"], d["target"], d["loss"], dloss, dXc, dE, wsb,
+                                        v_valid=v_valid, t=t, d_status=step.status)
+        fn()
+        ce_ms[mode] = event_median(fn, reps, flush)
+        step.check_status()
+        del wsb
+    ms = ce_ms["one_pass"]
     # vocab-parallel input embedding of the same T tokens (ids = the targets)
     emb = torch.empty(T, h, dtype=torch.bfloat16, device=d["Xc"].device)
     efn = lambda: mp.mp_vocab_embed(d["target"], d["E"], emb, v_valid=v_valid, t=t, d_status=step.status)
@@ -374,7 +381,8 @@ def time_next_rows(step, reps, flush):
     executed = 6.0 * T * h * v_pad  # plus the logit recompute (logits are never stored)
     return {"ce_bwd": {"ms": ms, "tflops_algorithmic": algo / (ms * 1e-3) / 1e12,
                        "tflops_executed": executed / (ms * 1e-3) / 1e12, "tokens_per_s": T / (ms * 1e-3),
-                       "launches": 1 + 3 * t,
+                       "workspace": "one pass (every shard's dZ, T*v_pad bf16); launches 4",
+                       "ms_shard_by_shard": ce_ms["shard_by_shard"], "launches_shard_by_shard": 1 + 3 * t,
                        "flop_note": "algorithmic 4*T*h*v_pad (dX, dE); executed adds the 2*T*h*v_pad recompute"},
             "vocab_embed": embed,
             "attn_fwd": attn}

@@ -32,7 +32,8 @@ STATUS_NAMES = {
 # Every symbol include/mptp.h declares.
 EXPORTS = ("mp_mlp_fwd", "mp_mlp_bwd", "mp_vocab_ce_workspace_bytes", "mp_vocab_ce", "mp_vocab_ce_partials",
            "mp_vocab_ce_combine", "mp_status_string", "mp_status_from_device", "mp_version",
-           "mp_vocab_ce_noalloc", "mp_vocab_ce_bwd_workspace_bytes", "mp_vocab_ce_bwd", "mp_vocab_embed",
+           "mp_vocab_ce_noalloc", "mp_vocab_ce_bwd_workspace_bytes", "mp_vocab_ce_bwd_workspace_bytes_one_pass",
+           "mp_vocab_ce_bwd", "mp_vocab_embed",
            "mp_attn_fwd")
 
 
@@ -69,6 +70,8 @@ def lib() -> ctypes.CDLL:
         L.mp_vocab_ce_combine.restype = _I
         L.mp_vocab_ce_bwd_workspace_bytes.argtypes = [_I, _I, _I, _I]
         L.mp_vocab_ce_bwd_workspace_bytes.restype = ctypes.c_size_t
+        L.mp_vocab_ce_bwd_workspace_bytes_one_pass.argtypes = [_I, _I, _I, _I]
+        L.mp_vocab_ce_bwd_workspace_bytes_one_pass.restype = ctypes.c_size_t
         L.mp_vocab_ce_bwd.argtypes = [_P] * 7 + [_P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P, _P]
         L.mp_vocab_ce_bwd.restype = _I
         L.mp_attn_fwd.argtypes = [_P] * 6 + [_I, _I, _I, _I, _I, _P, _P]
@@ -214,6 +217,10 @@ def mp_vocab_ce_noalloc(X, E, target, loss, *, v_valid: int, t: int, d_status=No
 
 def mp_vocab_ce_bwd_workspace_bytes(T: int, h: int, v_pad: int, t: int) -> int:
     return int(lib().mp_vocab_ce_bwd_workspace_bytes(int(T), int(h), int(v_pad), int(t)))
+
+
+def mp_vocab_ce_bwd_workspace_bytes_one_pass(T: int, h: int, v_pad: int, t: int) -> int:
+    return int(lib().mp_vocab_ce_bwd_workspace_bytes_one_pass(int(T), int(h), int(v_pad), int(t)))
 
 
 def mp_vocab_ce_bwd(X, E, target, loss, dloss, dX, dE, workspace, *, v_valid: int, t: int, d_status=None,

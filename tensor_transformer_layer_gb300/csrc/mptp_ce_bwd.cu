@@ -53,19 +53,23 @@ __global__ void __launch_bounds__(256) ce_lse_kernel(const __nv_bfloat16* __rest
     if (lane == 0) lse[r] = loss[r] + acc;
 }
 
+// Workspace: lse [T] fp32, then either (shard by shard, t > 1) an fp32 dX accumulator [T, h] and
+// one shard's dZ [T, v_pad / t] bf16, or (one pass, `chunks` = 1) every shard's dZ [T, v_pad] bf16.
 struct CeBwdLayout {
     size_t lse_off, acc_off, dz_off, total;
+    int chunks;  // vocabulary chunks processed one after another: t (shard by shard) or 1
 };
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-static bool ce_bwd_layout(int T, int h, int v_pad, int t, CeBwdLayout* L) {
+static bool ce_bwd_layout(int T, int h, int v_pad, int t, bool one_pass, CeBwdLayout* L) {
     if (T < 0 || h <= 0 || t < 1 || v_pad <= 0 || v_pad % (128 * t) != 0) return false;
-    const size_t vs = static_cast<size_t>(v_pad / t);
+    L->chunks = one_pass ? 1 : t;
+    const size_t vc = static_cast<size_t>(v_pad / L->chunks);
     L->lse_off = 0;
     L->acc_off = align256(size_t(T) * 4);
-    L->dz_off = L->acc_off + align256(size_t(T) * h * 4);
-    L->total = L->dz_off + align256(size_t(T) * vs * 2);
+    L->dz_off = L->acc_off + (L->chunks == 1 ? 0 : align256(size_t(T) * h * 4));  // one chunk: no accumulator
+    L->total = L->dz_off + align256(size_t(T) * vc * 2);
     return true;
 }
 
@@ -75,7 +79,13 @@ using namespace mptp;
 
 extern "C" size_t mp_vocab_ce_bwd_workspace_bytes(int T, int h, int v_pad, int t) {
     CeBwdLayout L;
-    if (!ce_bwd_layout(T, h, v_pad, t, &L)) return 0;
+    if (!ce_bwd_layout(T, h, v_pad, t, false, &L)) return 0;
+    return L.total;
+}
+
+extern "C" size_t mp_vocab_ce_bwd_workspace_bytes_one_pass(int T, int h, int v_pad, int t) {
+    CeBwdLayout L;
+    if (!ce_bwd_layout(T, h, v_pad, t, true, &L)) return 0;
     return L.total;
 }
 
@@ -91,9 +101,11 @@ extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const i
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return MP_ERR_MISALIGNED;
     if (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)) return MP_ERR_MISALIGNED;
-    CeBwdLayout lay;
-    ce_bwd_layout(T, h, v_pad, t, &lay);
+    CeBwdLayout lay, one;
+    ce_bwd_layout(T, h, v_pad, t, false, &lay);
+    ce_bwd_layout(T, h, v_pad, t, true, &one);
     if (T > 0 && workspace_bytes < lay.total) return MP_ERR_WORKSPACE;
+    if (workspace_bytes >= one.total) lay = one;  // room for every shard's dZ: one pass
     int sms = 0;
     mp_status st = check_device(&sms);
     if (st != MP_OK) return st;
@@ -112,10 +124,13 @@ extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const i
     ce_lse_kernel<<<ceil_div(T, 8), 256, 0, s>>>(Xb, Eb, target, loss, lse, T, h, v_valid, d_status);
     if (cudaGetLastError() != cudaSuccess) return MP_ERR_CUDA;
 
-    const int vs = v_pad / t;
+    // Vocabulary chunks of vs columns (whole shards, in shard order): one chunk when the
+    // workspace holds every shard's dZ, else one shard at a time.
+    const int C = lay.chunks;
+    const int vs = v_pad / C;
     const double Tb = 2.0 * T, hb = 2.0 * h, vb = 2.0 * vs;
     const unsigned long long budget = wait_budget_ns();
-    for (int i = 0; i < t; ++i) {
+    for (int i = 0; i < C; ++i) {
         const __nv_bfloat16* Ei = Eb + static_cast<long long>(i) * vs * h;
         __nv_bfloat16* dEi = reinterpret_cast<__nv_bfloat16*>(dE) + static_cast<long long>(i) * vs * h;
 
@@ -180,9 +195,9 @@ extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const i
         a12.pr.a_mn = 0;
         a12.pr.b_mn = b12f;
         a12.tiles_per_unit = 1;
-        a12.acc = acc;
+        a12.acc = C == 1 ? nullptr : acc;  // one pass: ACC_ONLY, no fp32 accumulator
         a12.ld_acc = h;
-        a12.acc_mode = (t == 1) ? ACC_ONLY : (i == 0 ? ACC_FIRST : (i == t - 1 ? ACC_LAST : ACC_MID));
+        a12.acc_mode = (C == 1) ? ACC_ONLY : (i == 0 ? ACC_FIRST : (i == C - 1 ? ACC_LAST : ACC_MID));
         a12.status = d_status;
         a12.budget_ns = budget;
         if (launch_gemm_tc<256, EPI_ACC, 4>(m12, a12, sms, s) != cudaSuccess) return MP_ERR_CUDA;

@@ -25,7 +25,7 @@ def _forward_loss(inp, v_valid, t):
     return loss
 
 
-def _run(inp, dloss, v_valid, t, expect_status=0, loss=None):
+def _run(inp, dloss, v_valid, t, expect_status=0, loss=None, one_pass=False):
     m = mp()
     X, E, tgt = inp["X"].cuda(), inp["E"].cuda(), inp["target"].cuda()
     T, h = X.shape
@@ -33,7 +33,8 @@ def _run(inp, dloss, v_valid, t, expect_status=0, loss=None):
     if loss is None:
         loss = _forward_loss(inp, v_valid, t)
     st = status_tensor()
-    wsb = torch.empty(m.mp_vocab_ce_bwd_workspace_bytes(T, h, v_pad, t), dtype=torch.uint8, device="cuda")
+    size = (m.mp_vocab_ce_bwd_workspace_bytes_one_pass if one_pass else m.mp_vocab_ce_bwd_workspace_bytes)
+    wsb = torch.empty(size(T, h, v_pad, t), dtype=torch.uint8, device="cuda")
     dX = torch.empty(T, h, dtype=torch.bfloat16, device="cuda")
     dE = torch.full((v_pad, h), 7.0, dtype=torch.bfloat16, device="cuda")
     m.mp_vocab_ce_bwd(X, E, tgt, loss, dloss.cuda(), dX, dE, wsb, v_valid=v_valid, t=t, d_status=st)
@@ -48,14 +49,31 @@ def _run(inp, dloss, v_valid, t, expect_status=0, loss=None):
     (257, 192, 2048, 1500, 8),     # the last shards hold only padding
     (130, 64, 1024, 1000, 1),      # one shard: dX stored straight from the accumulator
 ])
-def test_ce_bwd_matches_oracle(T, h, v_pad, v_valid, t):
+@pytest.mark.parametrize("one_pass", [False, True])
+def test_ce_bwd_matches_oracle(T, h, v_pad, v_valid, t, one_pass):
     inp = synth.ce_inputs(T, h, v_pad, v_valid, seed=8000 + T)
     dl = _dloss(T, 8100 + T)
-    dX, dE = _run(inp, dl, v_valid, t)
+    dX, dE = _run(inp, dl, v_valid, t, one_pass=one_pass)
     ref = oracle.ce_bwd(f64(inp["X"]), f64(inp["E"]), inp["target"].numpy(), dl.double().numpy(), v_valid)
     errs = {"dX": rel_fro(f64(dX), ref["dX"]), "dE": rel_fro(f64(dE), ref["dE"])}
     assert all(v <= GRAD_REL_FRO for v in errs.values()), errs
     assert torch.count_nonzero(dE[v_valid:]).item() == 0    # padding rows: zero gradient
+
+
+def test_ce_bwd_one_pass_against_shard_by_shard():
+    # With room for every shard's dZ the backward runs one GEMM of each kind: dE rows are the
+    # same K-loops (bitwise equal); dX sums the shards inside one K-loop instead of through an
+    # fp32 accumulator (equal within rounding).
+    m = mp()
+    T, h, v_pad, v_valid, t = 512, 192, 4096, 3900, 4
+    assert m.mp_vocab_ce_bwd_workspace_bytes_one_pass(T, h, v_pad, t) > m.mp_vocab_ce_bwd_workspace_bytes(T, h, v_pad, t)
+    inp = synth.ce_inputs(T, h, v_pad, v_valid, seed=8400)
+    dl = _dloss(T, 8401)
+    loss = _forward_loss(inp, v_valid, t)
+    dXs, dEs = _run(inp, dl, v_valid, t, loss=loss)
+    dXo, dEo = _run(inp, dl, v_valid, t, loss=loss, one_pass=True)
+    assert torch.equal(dEo, dEs)
+    assert rel_fro(f64(dXo), f64(dXs)) <= 1e-3
 
 
 def test_ce_bwd_shard_invariance():
@@ -79,7 +97,7 @@ def test_ce_bwd_1p2b_vocab_sampled():
     w = synth.WORKLOADS["ce_1p2b"]
     inp = synth.ce_inputs(w["T"], w["h"], w["v_pad"], w["v_valid"], w["seed"])
     dl = torch.full((w["T"],), 1.0 / w["T"], dtype=torch.float32)    # mean-loss gradient
-    dX, dE = _run(inp, dl, w["v_valid"], w["t"])
+    dX, dE = _run(inp, dl, w["v_valid"], w["t"], one_pass=True)
     rows = synth.sample_indices(w["T"], 64, seed=31).numpy()
     erows = np.unique(np.concatenate([synth.sample_indices(w["v_valid"], 60, seed=32).numpy(),
                                       np.array([50256, 50257, 51199])]))
