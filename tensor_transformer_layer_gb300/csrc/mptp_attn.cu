@@ -33,7 +33,8 @@
 //               is kept (P entries stay <= 256, and O and the sum use the same max, so
 //               the final quotient is unchanged). P = exp2(s log2(e)/sqrt(d) - m ...) is
 //               packed to bf16 and stored over the first 64 columns of S_g, where the next
-//               PV reads it. After the last tile O / l is read from TMEM and stored.
+//               PV reads it. After the last tile O / l is read from TMEM, staged in the
+//               shared memory of the group's Q tile (free by then) and written by TMA stores.
 // Key tiles above the diagonal are skipped; the diagonal tile is masked.
 #include <type_traits>
 
@@ -78,7 +79,8 @@ struct AttnArgs {
 
 template <int D>
 __global__ void __launch_bounds__(ATT_THREADS, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQKV, const AttnArgs args) {
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQKV, const __grid_constant__ CUtensorMap tmO,
+                    const AttnArgs args) {
     using Cfg = AttnCfg<D>;
     constexpr int NB = Cfg::NB;
     constexpr int KST = Cfg::KST, VST = Cfg::VST;
@@ -370,26 +372,38 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[g]);
         }
-        // O / l after the last PV.
+        // O / l after the last PV, through shared memory and TMA stores: each warp stages its 32
+        // rows as NB 32 x 32 boxes (64-byte swizzle: 16-byte piece j of row r at j ^ ((r >> 1) & 3))
+        // in the Q tile's space, which no product reads any more, and stores them whole.
         if (ok && ng > 0 && wait_all(&o_full[g], 0)) {
             tc_fence_after();
             const float inv = 1.0f / l;
-            uint4* dst = reinterpret_cast<uint4*>(args.O + static_cast<long long>(row_base + qt * ATT_BQ + qrow) * h +
-                                                  head * D);
+            uint8_t* stg = sQ + g * Cfg::Q_BYTES + q * (NB * 2048);
+            const int sw = (lane >> 1) & 3;
 #pragma unroll 1
             for (int c = 0; c < NB; ++c) {
                 uint32_t o[32];
                 tmem_ld32(o_addr + c * 32, o);
                 tmem_wait_ld();
                 reg_fence32(o);
+                uint8_t* row = stg + c * 2048 + lane * 64;
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
-                    dst[4 * c + v] = make_uint4(
+                    *reinterpret_cast<uint4*>(row + ((v ^ sw) << 4)) = make_uint4(
                         pack_bf16x2(__uint_as_float(o[8 * v]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
                         pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
                         pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
                         pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
             }
+            fence_proxy_async_smem();  // the stores are read by TMA (async proxy)
+            __syncwarp();
+            if (lane == 0) {
+                for (int c = 0; c < NB; ++c)
+                    tma_store_2d(&tmO, stg + c * 2048, head * D + c * 32, row_base + qt * ATT_BQ + q * 32);
+                bulk_commit_group();
+                bulk_wait_group<0>();  // written before the CTA exits
+            }
+            __syncwarp();
         }
     }
 
@@ -408,13 +422,13 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
 }
 
 template <int D>
-static cudaError_t launch_attn(const CUtensorMap& tmQKV, const AttnArgs& a, cudaStream_t s) {
+static cudaError_t launch_attn(const CUtensorMap& tmQKV, const CUtensorMap& tmO, const AttnArgs& a, cudaStream_t s) {
     using Cfg = AttnCfg<D>;
     auto kern = attn_fwd_kernel<D>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    kern<<<a.b * a.heads * a.npairs, ATT_THREADS, Cfg::SMEM_BYTES, s>>>(tmQKV, a);
+    kern<<<a.b * a.heads * a.npairs, ATT_THREADS, Cfg::SMEM_BYTES, s>>>(tmQKV, tmO, a);
     return cudaGetLastError();
 }
 
@@ -466,7 +480,9 @@ extern "C" mp_status mp_attn_fwd(const mp_bf16* X, const mp_bf16* Wqkv, const mp
 
     // Per-head causal attention.
     CUtensorMap tq;
-    if (!make_tmap_bf16_sw64(&tq, QKV, 3 * h, T, 3 * h, 32, ATT_BQ)) return MP_ERR_CUDA;
+    CUtensorMap to;  // O in 32 x 32 boxes, 64-byte swizzle (the kernel's staging layout)
+    if (!make_tmap_bf16_sw64(&tq, QKV, 3 * h, T, 3 * h, 32, ATT_BQ) || !make_tmap_bf16_out(&to, O, h, T, h))
+        return MP_ERR_CUDA;
     AttnArgs aa{};
     aa.O = reinterpret_cast<__nv_bfloat16*>(O);
     aa.b = b;
@@ -478,7 +494,7 @@ extern "C" mp_status mp_attn_fwd(const mp_bf16* X, const mp_bf16* Wqkv, const mp
     aa.scale_log2 = 1.4426950408889634f / sqrtf(static_cast<float>(d));
     aa.status = d_status;
     aa.budget_ns = budget;
-    cudaError_t e = d == 64 ? launch_attn<64>(tq, aa, cs) : launch_attn<96>(tq, aa, cs);
+    cudaError_t e = d == 64 ? launch_attn<64>(tq, to, aa, cs) : launch_attn<96>(tq, to, aa, cs);
     if (e != cudaSuccess) return MP_ERR_CUDA;
 
     // out = sum_i O_i Wo_i: the K-loop runs over the heads' columns in ascending order, i.e.
