@@ -63,6 +63,20 @@ def test_workspace_bytes(L):
     assert mp.mp_vocab_ce_workspace_bytes(0, 1024, 1) == 0
 
 
+def test_ce_bwd_workspace_bytes(L):
+    import tensor_transformer_layer_gb300 as mp
+    a256 = lambda x: (x + 255) // 256 * 256
+    T, h, v_pad, t = 8192, 1536, 51200, 8
+    # shard by shard: lse [T] fp32, fp32 dX accumulator [T, h], one shard of dZ [T, v_pad/t] bf16
+    assert mp.mp_vocab_ce_bwd_workspace_bytes(T, h, v_pad, t) == a256(T * 4) + a256(T * h * 4) + a256(T * 6400 * 2)
+    # one pass: lse and every shard's dZ [T, v_pad] bf16
+    assert mp.mp_vocab_ce_bwd_workspace_bytes_one_pass(T, h, v_pad, t) == a256(T * 4) + a256(T * v_pad * 2)
+    # one shard: the two layouts coincide (no accumulator)
+    assert (mp.mp_vocab_ce_bwd_workspace_bytes(300, 128, 2048, 1) ==
+            mp.mp_vocab_ce_bwd_workspace_bytes_one_pass(300, 128, 2048, 1) == a256(300 * 4) + a256(300 * 2048 * 2))
+    assert mp.mp_vocab_ce_bwd_workspace_bytes_one_pass(10, 64, 1000, 8) == 0   # v_pad not a multiple of 128 t
+
+
 FAKE = ctypes.c_void_p(0x100000)  # never dereferenced: every call below fails validation first
 
 
