@@ -107,14 +107,15 @@ def test_ce_bwd_1p2b_vocab_sampled():
     assert all(v <= GRAD_REL_FRO for v in errs.values()), errs
 
 
-def test_ce_bwd_invalid_target_contributes_nothing():
+@pytest.mark.parametrize("one_pass", [False, True])
+def test_ce_bwd_invalid_target_contributes_nothing(one_pass):
     m = mp()
     inp = synth.ce_inputs(64, 64, 1024, 1000, seed=8300)
     dl = _dloss(64, 8301)
     tgt = inp["target"].clone()
     tgt[7] = 1000
     inp["target"] = tgt
-    dX, dE = _run(inp, dl, 1000, 2, expect_status=m.MP_DEV_TARGET_RANGE)
+    dX, dE = _run(inp, dl, 1000, 2, expect_status=m.MP_DEV_TARGET_RANGE, one_pass=one_pass)
     keep = np.ones(64, dtype=bool)
     keep[7] = False
     ref = oracle.ce_bwd(f64(inp["X"])[keep], f64(inp["E"]), tgt.numpy()[keep], dl.double().numpy()[keep], 1000)
