@@ -354,9 +354,16 @@ def time_next_rows(step, reps, flush):
     efn()
     ems = event_median(efn, reps, flush)
     ebytes = 2.0 * T * h * 2 + 4.0 * T   # read T rows of E, write T rows, read the ids
+    # context: a plain device copy of the same T x h bf16 rows, timed the same way (a 50 MB
+    # kernel is dominated by its ramp and by the flush's dirty lines written back under it)
+    csrc_ = torch.empty(T, h, dtype=torch.bfloat16, device=d["Xc"].device)
+    cdst = torch.empty_like(csrc_)
+    cms = event_median(lambda: cdst.copy_(csrc_), reps, flush)
+    del csrc_, cdst
     peaks, peak_src = load_peaks()
     embed = {"ms": ems, "gbs": ebytes / (ems * 1e-3) / 1e9, "bytes": ebytes,
-             "frac_of_hbm": ebytes / (ems * 1e-3) / 1e9 / peaks["hbm_gbs"], "hbm_peak_source": peak_src}
+             "frac_of_hbm": ebytes / (ems * 1e-3) / 1e9 / peaks["hbm_gbs"], "hbm_peak_source": peak_src,
+             "torch_copy_same_bytes_ms": cms, "vs_torch_copy": cms / ems}
     # head-parallel causal attention block at the 8.3B-layer shape (b = 4, s = 1024, 32 heads of 96, t = 8)
     import synth
     ab, as_, ah, aheads, at = 4, 1024, MLP["h"], 32, MLP["t"]
