@@ -15,7 +15,7 @@
 // 2p and 2p+1), 384 threads, the longest pairs launched first. The two query tiles
 // ("A" = 2p, "B" = 2p+1) share every K and V tile they both need (causal: keys 0..2p for
 // A, 0..2p+1 for B), so each K/V tile is loaded once for 256 queries.
-//   warpgroup 0 (64 registers a thread): warp 0 is the TMA producer: both Q tiles once, then
+//   warpgroup 0 (64 or 72 registers a thread): warp 0 is the TMA producer: both Q tiles once, then
 //               K tiles into a ring that runs ahead and V tiles into a ring of their own
 //               (head width D loaded as D/32 boxes of 32 columns, 64-byte swizzle). Warp 1
 //               allocates TMEM and issues the products: the whole warp runs the issue loop
@@ -24,7 +24,7 @@
 //               (D columns, at 256 and 384). Per key tile j and query tile g it issues
 //               PV_g(j) (O_g += P_g V_j, P_g read from TMEM) and then S_g(j+1) = Q_g K_{j+1}^T;
 //               while one tile's softmax runs, the tensor core works on the other tile.
-//   warpgroups 1, 2 (216 registers a thread): softmax of tile A and of tile B; thread =
+//   warpgroups 1, 2 (216 or 208 registers a thread): softmax of tile A and of tile B; thread =
 //               query row (the TMEM lane quarter of the warp), all 128 key columns. The
 //               score row is read from TMEM once; row max over four chains of three-input
 //               maxima. The running max is raised lazily: only when it grows by more than
@@ -46,8 +46,6 @@ namespace mptp {
 constexpr int ATT_BQ = 128;   // queries per tile (two tiles per CTA)
 constexpr int ATT_BKV = 128;  // keys per tile
 constexpr int ATT_THREADS = 384;  // warpgroup 0: TMA, MMA, two idle warps; 1, 2: softmax
-constexpr int ATT_REGS_CTRL = 64;    // registers per thread in warpgroup 0
-constexpr int ATT_REGS_SOFTMAX = 216;  // in the softmax warpgroups: 128 x 64 + 256 x 216 <= 384 x 168
 constexpr float ATT_RESCALE_LOG2 = 8.0f;  // lazy rescale threshold on the max, exp2 domain
 
 template <int D>
@@ -57,6 +55,12 @@ struct AttnCfg {
     static constexpr int BOX_BYTES = 128 * 64;            // 128 rows x 32 bf16
     static constexpr int Q_BYTES = NB * BOX_BYTES;        // one query tile
     static constexpr int KV_TILE_BYTES = NB * BOX_BYTES;  // one K or one V tile
+    // Registers a thread in warpgroup 0 and in the softmax warpgroups (setmaxnreg); the launch
+    // gives 384 x 168, so 128 x REGS_CTRL + 256 x REGS_SOFTMAX must not exceed it. The splits
+    // without spills: the MMA issuer needs more than 64 at D = 96 (six-step products).
+    static constexpr int REGS_CTRL = D == 64 ? 64 : 72;
+    static constexpr int REGS_SOFTMAX = D == 64 ? 216 : 208;
+    static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= ATT_THREADS * 168, "register split");
     static constexpr int KST = D == 64 ? 4 : 3;           // K ring stages
     static constexpr int VST = D == 64 ? 4 : 3;           // V ring stages
     // q_full, K ring, V ring, s_full/p_full/o_full per query tile, drain
@@ -152,7 +156,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const Ctl ctl{args.status, abort_flag, args.budget_ns};
 
     if (warp < 4) {
-        reg_dealloc<ATT_REGS_CTRL>();
+        reg_dealloc<Cfg::REGS_CTRL>();
         if (warp == 0) {
             if (lane == 0) {
                 // ---------------- TMA producer ----------------
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
             wait_drain(drain_bar, 0, args.status);
         }
     } else {
-        reg_alloc<ATT_REGS_SOFTMAX>();
+        reg_alloc<Cfg::REGS_SOFTMAX>();
         // ---------------- softmax (warps 4..7: tile A, 8..11: tile B) ----------------
         const int g = (warp - 4) >> 2;
         const int q = warp & 3;                         // TMEM lane quarter

@@ -42,8 +42,10 @@ def _run(inp, b, s, heads, t):
     (1, 512, 384, 4, 4),      # d = 96, four tiles (causal skipping and the diagonal)
     (3, 128, 128, 2, 1),      # d = 64, one tile
     (2, 384, 256, 4, 2),      # d = 64
-    (8, 1024, 512, 8, 2),     # d = 64, 512 work items: several per CTA of the persistent grid
+    (8, 1024, 512, 8, 2),     # d = 64, 512 work items (more than three waves)
     (6, 768, 768, 8, 4),      # d = 96, 288 work items of 1..6 key tiles
+    (2, 384, 192, 2, 1),      # d = 96, odd tile count: a pair with one query tile
+    (1, 128, 192, 2, 1),      # d = 96, a single query tile
 ])
 def test_attn_matches_oracle(b, s, h, heads, t):
     inp = _inputs(b, s, h, seed=10000 + s + h)
