@@ -154,6 +154,9 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const Ctl ctl{args.status, abort_flag, args.budget_ns};
+    // Launched as the QKV GEMM's programmatic dependent: QKV is read only after that grid completes.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp < 4) {
         reg_dealloc<Cfg::REGS_CTRL>();
@@ -432,8 +435,8 @@ static cudaError_t launch_attn(const CUtensorMap& tmQKV, const CUtensorMap& tmO,
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    kern<<<a.b * a.heads * a.npairs, ATT_THREADS, Cfg::SMEM_BYTES, s>>>(tmQKV, tmO, a);
-    return cudaGetLastError();
+    e = launch_pdl(kern, dim3(a.b * a.heads * a.npairs), dim3(ATT_THREADS), Cfg::SMEM_BYTES, s, tmQKV, tmO, a);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mptp

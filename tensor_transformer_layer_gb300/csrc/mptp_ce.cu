@@ -16,6 +16,7 @@ namespace mptp {
 __global__ void __launch_bounds__(128) ce_combine_kernel(const float* __restrict__ ws, const int32_t* __restrict__ target,
                                                          float* __restrict__ loss, int T, int P, int chunk_cols,
                                                          int v_valid, uint32_t* status) {
+    grid_dependency_wait();  // the partials of the logit GEMM before it
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= T) return;
     const long long stride = 3ll * T;
@@ -126,9 +127,10 @@ extern "C" mp_status mp_vocab_ce_combine(const void* workspace, size_t workspace
     CePlan plan;
     ce_plan(v_pad, t, &plan);
     const int threads = 128;
-    ce_combine_kernel<<<ceil_div(T, threads), threads, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const float*>(workspace), target, loss, T, plan.P, plan.chunk_cols, v_valid, d_status);
-    return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+    const cudaError_t e = launch_pdl(ce_combine_kernel, dim3(ceil_div(T, threads)), dim3(threads), 0,
+                                     static_cast<cudaStream_t>(stream), static_cast<const float*>(workspace), target,
+                                     loss, T, plan.P, plan.chunk_cols, v_valid, d_status);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
 }
 
 extern "C" mp_status mp_vocab_ce(const mp_bf16* X, const mp_bf16* E, const int32_t* target, float* loss,

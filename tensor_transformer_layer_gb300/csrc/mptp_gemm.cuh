@@ -359,6 +359,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const Ctl ctl{args.status, abort_flag, args.budget_ns};
+    // The set-up above overlaps the previous kernel's tail when this grid was launched as its
+    // programmatic dependent; no global memory is touched before the previous grid completes.
+    grid_dependency_wait();
+    grid_launch_dependents();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -766,6 +770,30 @@ inline bool balance_pairs() {
     return !(v != nullptr && v[0] == '0');
 }
 
+// MPTP_PDL=0 launches the GEMMs without programmatic stream serialization.
+inline bool pdl_enabled() {
+    const char* v = std::getenv("MPTP_PDL");
+    return !(v != nullptr && v[0] == '0');
+}
+
+// Launch with programmatic stream serialization: the kernel may start while the previous kernel
+// in the stream is finishing, and waits for it (grid_dependency_wait) before touching global
+// memory. Cluster dimensions come from the kernel's own attribute.
+template <typename Kern, typename... Args>
+inline cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Host-side launcher: grid = 2 x min(units, resident pairs, max_pairs if > 0), one CTA per SM.
 template <int BN, int EPI, int NE>
 inline cudaError_t launch_gemm_tc(const TmapSet& maps, const GemmArgs& args, int num_sms, cudaStream_t stream,
@@ -787,8 +815,8 @@ inline cudaError_t launch_gemm_tc(const TmapSet& maps, const GemmArgs& args, int
         use = (args.pr.num_units + rounds - 1) / rounds;
     }
     if (use <= 0) return cudaSuccess;
-    kern<<<2 * use, Cfg::NUM_THREADS, Cfg::SMEM_BYTES, stream>>>(maps, args);
-    return cudaGetLastError();
+    e = launch_pdl(kern, dim3(2 * use), dim3(Cfg::NUM_THREADS), Cfg::SMEM_BYTES, stream, maps, args);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace mptp

@@ -158,6 +158,14 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// Programmatic dependent launch. A grid launched with programmatic stream serialization may
+// start before the previous kernel in its stream has finished; grid_dependency_wait() blocks
+// until every grid it depends on has completed and its memory operations are visible (it
+// returns at once when there is no such dependency). grid_launch_dependents() lets the next
+// such grid in the stream start launching once every CTA of this one has signalled or exited.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
