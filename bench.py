@@ -325,6 +325,22 @@ def time_breakdown(step, reps, flush):
     return {name: round(event_median(fn, reps, flush), 4) for name, fn in calls.items()}
 
 
+def combine_row(ms, peaks, peak_src):
+    """The step's one memory-bound kernel, the cross-entropy combine (K7), against the measured
+    HBM copy bandwidth. Algorithmic bytes: the (max, sum-exp) planes of every partition, one
+    target logit, the target and the loss per token."""
+    import tensor_transformer_layer_gb300 as mp
+    T = CE["T"]
+    P = mp.mp_vocab_ce_workspace_bytes(T, CE["v_pad"], CE["t"]) // (12 * T)
+    nbytes = 8 * T * P + 12 * T
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"kernel": "K7 cross-entropy combine (mp_vocab_ce_combine)", "bound": "hbm", "bytes": nbytes,
+            "partitions": P, "ms": ms, "achieved_gbs": gbs, "peak_gbs": peaks["hbm_gbs"],
+            "frac": gbs / peaks["hbm_gbs"], "peak_source": peak_src,
+            "timing": "CUDA events around one call after an L2 flush (launch included); at a few MB the "
+                      "kernel is bound by DRAM latency and the launch, not bandwidth"}
+
+
 def time_next_rows(step, reps, flush):
     """Rows beyond the step (measured beside it, not inside `value`): the fused
     vocab-parallel cross-entropy backward on the step's CE workload."""
@@ -690,6 +706,7 @@ def main(argv=None):
             "breakdown_ms": breakdown,
             "next_rows": next_rows,
             "torch_context": context,
+            "memory_bound": combine_row(breakdown["ce_combine"], peaks, peak_src),
             "roofline": {"kernel": "mp_vocab_ce_partials (logit GEMM + online LSE epilogue)", "bound": "tensor",
                          "achieved": ce_achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                          "frac": ce_achieved / peaks["bf16_tflops_sustained"],

@@ -13,35 +13,74 @@
 
 namespace mptp {
 
-__global__ void __launch_bounds__(128) ce_combine_kernel(const float* __restrict__ ws, const int32_t* __restrict__ target,
-                                                         float* __restrict__ loss, int T, int P, int chunk_cols,
-                                                         int v_valid, uint32_t* status) {
+// K7 layout: lane = token (every load of a partition plane is one coalesced 128-byte line per
+// warp). A block's W warps (W = 8 when G = 8, else 4) form W / G token groups of 32 tokens, and
+// the G warps of a group split the partitions (share j takes j, j + G, j + 2G, ...). With few
+// tokens G = 8 puts every partition's load in flight at once; with many, G = 1 is one thread
+// per token over all partitions. Each warp issues CMB_LOADS partitions' loads before reducing
+// them; a group's G partial (max, sum) pairs are merged in shared memory.
+constexpr int CMB_WARPS = 8;  // warps per block at most
+constexpr int CMB_LOADS = 8;  // partitions a warp loads before reducing them
+
+// Fold partials (m_j, s_j) into the running (M, S): M = max, S = sum s_j exp(m_j - M), the
+// running sum rescaled when M grows; partitions with no valid column (s = 0, m = -inf) skip.
+__device__ __forceinline__ void lse_fold(float& M, float& S, const float (&mm)[CMB_LOADS], const float (&ss)[CMB_LOADS]) {
+    float cm = mm[0];
+#pragma unroll
+    for (int j = 1; j < CMB_LOADS; ++j) cm = fmaxf(cm, mm[j]);
+    const float nM = fmaxf(M, cm);
+    if (nM == -INFINITY) return;
+    S = (M == -INFINITY) ? 0.0f : S * expf(M - nM);
+#pragma unroll
+    for (int j = 0; j < CMB_LOADS; ++j)
+        if (ss[j] > 0.0f) S += ss[j] * expf(mm[j] - nM);
+    M = nM;
+}
+
+// SPLIT = false is the G = 1 form (no merge, fewer registers, more resident threads).
+template <bool SPLIT>
+__global__ void __launch_bounds__(32 * CMB_WARPS) ce_combine_kernel(const float* __restrict__ ws,
+                                                                    const int32_t* __restrict__ target,
+                                                                    float* __restrict__ loss, int T, int P, int G,
+                                                                    int chunk_cols, int v_valid, uint32_t* status) {
     grid_dependency_wait();  // the partials of the logit GEMM before it
-    const int r = blockIdx.x * blockDim.x + threadIdx.x;
-    if (r >= T) return;
+    __shared__ float sM[SPLIT ? CMB_WARPS : 1][32], sS[SPLIT ? CMB_WARPS : 1][32];
+    if (!SPLIT) G = 1;
+    const int lane = threadIdx.x & 31;
+    const int w = threadIdx.x >> 5;
+    const int grp = w / G, share = w % G;
+    const int r = (blockIdx.x * (static_cast<int>(blockDim.x >> 5) / G) + grp) * 32 + lane;
+    const bool valid = r < T;
     const long long stride = 3ll * T;
-    // One pass over the partitions, 8 at a time (independent loads in flight):
-    // M = max_p m_p, S = sum_p s_p exp(m_p - M) with the running sum rescaled when M
-    // grows; partitions holding no valid column (s_p = 0, m_p = -inf) are skipped.
     float M = -INFINITY, S = 0.0f;
-    for (int p0 = 0; p0 < P; p0 += 8) {
-        float mm[8], ss[8];
+    if (valid) {
+        for (int p0 = share; p0 < P; p0 += G * CMB_LOADS) {
+            float mm[CMB_LOADS], ss[CMB_LOADS];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int p = p0 + j;
-            mm[j] = (p < P) ? ws[p * stride + r] : -INFINITY;
-            ss[j] = (p < P) ? ws[p * stride + T + r] : 0.0f;
+            for (int j = 0; j < CMB_LOADS; ++j) {
+                const int p = p0 + j * G;
+                mm[j] = (p < P) ? ws[p * stride + r] : -INFINITY;
+                ss[j] = (p < P) ? ws[p * stride + T + r] : 0.0f;
+            }
+            lse_fold(M, S, mm, ss);
         }
-        float cm = mm[0];
+    }
+    if constexpr (SPLIT) {
+        sM[w][lane] = M;
+        sS[w][lane] = S;
+        __syncthreads();
+        if (share != 0 || !valid) return;
+        float mm[CMB_LOADS], ss[CMB_LOADS];
 #pragma unroll
-        for (int j = 1; j < 8; ++j) cm = fmaxf(cm, mm[j]);
-        const float nM = fmaxf(M, cm);
-        if (nM == -INFINITY) continue;
-        S = (M == -INFINITY) ? 0.0f : S * expf(M - nM);
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (ss[j] > 0.0f) S += ss[j] * expf(mm[j] - nM);
-        M = nM;
+        for (int j = 0; j < CMB_LOADS; ++j) {
+            mm[j] = j < G ? sM[w + j][lane] : -INFINITY;
+            ss[j] = j < G ? sS[w + j][lane] : 0.0f;
+        }
+        M = -INFINITY;
+        S = 0.0f;
+        lse_fold(M, S, mm, ss);
+    } else if (!valid) {
+        return;
     }
     const int tg = target[r];
     if (tg < 0 || tg >= v_valid) {
@@ -51,6 +90,17 @@ __global__ void __launch_bounds__(128) ce_combine_kernel(const float* __restrict
     }
     const float z = ws[(tg / chunk_cols) * stride + 2ll * T + r];
     loss[r] = M + logf(S) - z;
+}
+static_assert(CMB_WARPS <= CMB_LOADS, "a group's merge folds up to CMB_WARPS pairs in one pass");
+
+// Warps per token group: the largest of 1, 2, 4, 8 that keeps the grid within about 27 warps a
+// SM (measured on T = 8192, 32768 and 131172 tokens with 40 partitions: splitting further only
+// adds blocks once the loads in flight already cover the DRAM latency).
+static int combine_group(long long T, int sms) {
+    const long long token_warps = (T + 31) / 32;
+    int G = CMB_WARPS;
+    while (G > 1 && token_warps * G > 27ll * sms) G >>= 1;
+    return G;
 }
 
 static mp_status check_ce_shape(int T, int h, int v_pad, int v_valid, int t) {
@@ -126,10 +176,12 @@ extern "C" mp_status mp_vocab_ce_combine(const void* workspace, size_t workspace
     if (st != MP_OK) return st;
     CePlan plan;
     ce_plan(v_pad, t, &plan);
-    const int threads = 128;
-    const cudaError_t e = launch_pdl(ce_combine_kernel, dim3(ceil_div(T, threads)), dim3(threads), 0,
-                                     static_cast<cudaStream_t>(stream), static_cast<const float*>(workspace), target,
-                                     loss, T, plan.P, plan.chunk_cols, v_valid, d_status);
+    const int G = combine_group(T, sms);
+    const int W = G == CMB_WARPS ? CMB_WARPS : 4;  // warps per block
+    const cudaError_t e = launch_pdl(G > 1 ? ce_combine_kernel<true> : ce_combine_kernel<false>,
+                                     dim3(ceil_div(T, 32 * (W / G))), dim3(32 * W),
+                                     0, static_cast<cudaStream_t>(stream), static_cast<const float*>(workspace),
+                                     target, loss, T, plan.P, G, plan.chunk_cols, v_valid, d_status);
     return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
 }
 
