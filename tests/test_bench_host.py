@@ -77,3 +77,16 @@ def test_reference_arm_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
     assert line["metric"] == bench.METRIC
+
+
+def test_combine_row_bytes():
+    # The combine reads the (max, sum-exp) planes of every partition (2 P T floats), the
+    # target and one target logit per token, and writes the loss: 8 P T + 12 T bytes.
+    import tensor_transformer_layer_gb300 as mp
+    T = bench.CE["T"]
+    P = mp.mp_vocab_ce_workspace_bytes(T, bench.CE["v_pad"], bench.CE["t"]) // (12 * T)
+    assert P * 12 * T == mp.mp_vocab_ce_workspace_bytes(T, bench.CE["v_pad"], bench.CE["t"])
+    row = bench.combine_row(0.01, {"hbm_gbs": 5000.0}, "test")
+    assert row["bytes"] == 8 * P * T + 12 * T and row["partitions"] == P
+    assert abs(row["achieved_gbs"] - row["bytes"] / 1e-5 / 1e9) < 1e-6
+    assert abs(row["frac"] - row["achieved_gbs"] / 5000.0) < 1e-12 and row["bound"] == "hbm"
