@@ -36,6 +36,11 @@
  *     MPTP_WAIT_BUDGET_NS overrides); when a bound runs out the kernel sets
  *     MP_DEV_TIMEOUT, lets its own copies and MMAs in flight finish, frees its
  *     tensor memory and returns. Outputs are then undefined.
+ *   - Kernels are launched with programmatic stream serialization: a kernel may
+ *     begin its set-up while the previous kernel in the stream finishes, and
+ *     reads or writes global memory only after that kernel has completed, so
+ *     stream order and CUDA-graph capture behave as for plain launches.
+ *     MPTP_PDL=0 launches them plainly.
  *   - Outputs are overwritten, never accumulated into. T = 0 is a valid no-op.
  *   - Results are deterministic: no atomics in any reduction, fixed order.
  */
