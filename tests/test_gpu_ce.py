@@ -100,3 +100,18 @@ def test_ce_workspace_too_small():
     with pytest.raises(m.MptpError) as e:
         m.mp_vocab_ce(X, E, tgt, loss, ws, v_valid=1000, t=2)
     assert e.value.code == 8
+
+
+@pytest.mark.parametrize("T", [20000, 40000, 70000, 70001])
+def test_ce_combine_group_sizes(T):
+    # The combine splits each 32-token group's 16 partitions over G warps, G from the token count
+    # (here 4, 2, 1 and 1 with a ragged last warp); sampled tokens (the first and last groups
+    # among them) against the oracle.
+    h, v_pad, v_valid, t = 64, 16384, 16000, 8
+    inp = synth.ce_inputs(T, h, v_pad, v_valid, seed=4700 + T)
+    got = run_ce(inp, v_valid, t)
+    rows = np.unique(np.concatenate([np.arange(40), synth.sample_indices(T, 48, seed=5).numpy(),
+                                     np.arange(T - 40, T)]))
+    want = oracle.ce_loss(f64(inp["X"])[rows], f64(inp["E"]), inp["target"].numpy()[rows], v_valid)
+    assert float(np.max(np.abs(got[rows] - want))) <= LOSS_ABS
+    assert np.all(np.isfinite(got))
