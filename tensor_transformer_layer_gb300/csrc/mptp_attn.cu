@@ -122,6 +122,15 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     const int row_base = seq * args.s;          // first token row of this sequence
     const int h = args.h;
 
+    constexpr int LEAD = KST - 1;  // K tiles loaded ahead of the V tile of the same index
+    // Tile j of K (column block 1 of QKV) or V (block 2) into ring stage st, once the stage is free.
+    auto issue_kv = [&](int j, int which, uint64_t* full, uint8_t* ring, int st) {
+        mbar_arrive_expect_tx(&full[st], Cfg::KV_TILE_BYTES);
+        uint8_t* dst = ring + st * Cfg::KV_TILE_BYTES;
+        for (int c = 0; c < NB; ++c)
+            tma_load_2d(dst + c * Cfg::BOX_BYTES, &tmQKV, &full[st], which * h + head * D + c * 32,
+                        row_base + j * ATT_BKV);
+    };
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(drain_bar, 1);
@@ -141,9 +150,19 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         *abort_flag = 0u;
         fence_mbarrier_init();
         fence_proxy_async_smem();
-    }
-    if (warp == 0 && lane == 0) {
+        // The producer thread issues the first loads (both Q tiles and the first LEAD K tiles,
+        // whose ring stages are still free) now, so that their latency overlaps the rest of the
+        // set-up; QKV is read only once the grid that writes it has completed.
         prefetch_tensormap(&tmQKV);
+        grid_dependency_wait();
+        mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * Cfg::Q_BYTES);
+        for (int c = 0; c < NB; ++c)
+            tma_load_2d(sQ + c * Cfg::BOX_BYTES, &tmQKV, q_full, head * D + c * 32, row_base + qt_a * ATT_BQ);
+        if (has_b)
+            for (int c = 0; c < NB; ++c)
+                tma_load_2d(sQ + Cfg::Q_BYTES + c * Cfg::BOX_BYTES, &tmQKV, q_full, head * D + c * 32,
+                            row_base + qt_b * ATT_BQ);
+        for (int j = 0; j < LEAD && j < n; ++j) issue_kv(j, 1, k_full, sK, j);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -163,27 +182,14 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         if (warp == 0) {
             if (lane == 0) {
                 // ---------------- TMA producer ----------------
-                mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * Cfg::Q_BYTES);
-                for (int c = 0; c < NB; ++c)
-                    tma_load_2d(sQ + c * Cfg::BOX_BYTES, &tmQKV, q_full, head * D + c * 32, row_base + qt_a * ATT_BQ);
-                if (has_b)
-                    for (int c = 0; c < NB; ++c)
-                        tma_load_2d(sQ + Cfg::Q_BYTES + c * Cfg::BOX_BYTES, &tmQKV, q_full, head * D + c * 32,
-                                    row_base + qt_b * ATT_BQ);
-                // Tile j of K (column block 1 of QKV) or V (block 2) into a ring stage.
+                // (Both Q tiles and K tiles 0 .. LEAD - 1 went out during the set-up.)
                 auto load = [&](int j, int which, uint64_t* full, uint64_t* empty, uint8_t* ring, int stages) -> bool {
                     const int st = j % stages;
                     if (!wait_bounded(&empty[st], ((j / stages) & 1) ^ 1u, ctl)) return false;
-                    mbar_arrive_expect_tx(&full[st], Cfg::KV_TILE_BYTES);
-                    uint8_t* dst = ring + st * Cfg::KV_TILE_BYTES;
-                    for (int c = 0; c < NB; ++c)
-                        tma_load_2d(dst + c * Cfg::BOX_BYTES, &tmQKV, &full[st], which * h + head * D + c * 32,
-                                    row_base + j * ATT_BKV);
+                    issue_kv(j, which, full, ring, st);
                     return true;
                 };
-                constexpr int LEAD = KST - 1;  // K tiles loaded ahead of the V tile of the same index
                 bool ok = true;
-                for (int j = 0; j < LEAD && j < n && ok; ++j) ok = load(j, 1, k_full, k_empty, sK, KST);
                 for (int j = 0; j < n && ok; ++j) {
                     if (j + LEAD < n) ok = load(j + LEAD, 1, k_full, k_empty, sK, KST);
                     if (ok) ok = load(j, 2, v_full, v_empty, sV, VST);
