@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(256) ce_lse_kernel(const __nv_bfloat16* __rest
                                                      const int32_t* __restrict__ target,
                                                      const float* __restrict__ loss, float* __restrict__ lse, int T,
                                                      int h, int v_valid, uint32_t* status) {
+    grid_dependency_wait();  // the kernels that wrote the loss (and X) before it
+    grid_launch_dependents();
     const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (r >= T) return;
@@ -121,8 +123,10 @@ extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const i
     const __nv_bfloat16* Xb = reinterpret_cast<const __nv_bfloat16*>(X);
     const __nv_bfloat16* Eb = reinterpret_cast<const __nv_bfloat16*>(E);
 
-    ce_lse_kernel<<<ceil_div(T, 8), 256, 0, s>>>(Xb, Eb, target, loss, lse, T, h, v_valid, d_status);
-    if (cudaGetLastError() != cudaSuccess) return MP_ERR_CUDA;
+    if (launch_pdl(ce_lse_kernel, dim3(ceil_div(T, 8)), dim3(256), 0, s, Xb, Eb, target, loss, lse, T, h, v_valid,
+                   d_status) != cudaSuccess ||
+        cudaGetLastError() != cudaSuccess)
+        return MP_ERR_CUDA;
 
     // Vocabulary chunks of vs columns (whole shards, in shard order): one chunk when the
     // workspace holds every shard's dZ, else one shard at a time.
