@@ -45,7 +45,7 @@ MLP = dict(T=4096, h=3072, f=12288, t=8, seed=1003)
 CE = dict(T=8192, h=1536, v_pad=51200, v_valid=50257, t=8, seed=1002)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS_PER_STEP = 8  # fwd: 2, bwd: 4, CE: 2
-KERNEL_SOURCES = ("mptp_gemm.cuh", "mptp_ptx.cuh", "mptp_ce.cu")
+KERNEL_SOURCES = ("mptp_gemm.cuh", "mptp_ptx.cuh", "mptp_launch.cuh", "mptp_ce.cu")
 
 
 def mlp_flop(w=MLP):

@@ -10,6 +10,8 @@
 #include <cuda_bf16.h>
 
 #include "mptp_internal.h"
+#include "mptp_launch.cuh"
+#include "mptp_ptx.cuh"
 
 namespace mptp {
 
@@ -17,6 +19,8 @@ __global__ void __launch_bounds__(256) vocab_embed_kernel(const int32_t* __restr
                                                           const uint4* __restrict__ E, uint4* __restrict__ out,
                                                           int T, int hv, int vs, int t, int v_valid,
                                                           uint32_t* status) {
+    grid_dependency_wait();  // the kernels that wrote the ids (or E) before it
+    grid_launch_dependents();
     const int warps = (gridDim.x * blockDim.x) >> 5;
     const int lane = threadIdx.x & 31;
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < T; r += warps) {
@@ -65,8 +69,8 @@ extern "C" mp_status mp_vocab_embed(const int32_t* ids, const mp_bf16* E, mp_bf1
     if (st != MP_OK) return st;
     const int blocks_needed = ceil_div(T, 8);
     const int grid = blocks_needed < sms * 8 ? blocks_needed : sms * 8;
-    vocab_embed_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        ids, reinterpret_cast<const uint4*>(E), reinterpret_cast<uint4*>(out), T, h / 8, v_pad / t, t, v_valid,
-        d_status);
-    return cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+    const cudaError_t e = launch_pdl(vocab_embed_kernel, dim3(grid), dim3(256), 0, static_cast<cudaStream_t>(stream), ids,
+                                     reinterpret_cast<const uint4*>(E), reinterpret_cast<uint4*>(out), T, h / 8,
+                                     v_pad / t, t, v_valid, d_status);
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
 }
