@@ -16,6 +16,12 @@ per-step CUDA events. `e2e` repeats the step through the same C-ABI calls with
 pinned HOST buffers, the host-to-device copies of the inputs and the
 device-to-host copies of the results inside the timed region.
 
+Beside the timed steps (never inside `value`): `sustained` runs the same step back
+to back for several seconds, long enough for the board's power cap to set the
+clock, with the SM clock sampled and each chunk of steps binned by the clock it
+ran at; `ce_8p3b` times the fused cross-entropy at the 8.3B-layer width (T = 4096,
+h = 3072, the same vocabulary and t = 8) with its own roofline entry.
+
 `--impl reference` times the float64 CPU oracle on bounded token samples of the
 same workload instead (the reference arm); `cpu_baseline` in the main line is
 the same oracle timed once on a bounded sample.
@@ -43,6 +49,9 @@ if ROOT not in sys.path:
 METRIC = "TFLOP/s and % of GB300 BF16 tensor peak: sharded MLP fwd+bwd; vocab-CE tokens/s"
 MLP = dict(T=4096, h=3072, f=12288, t=8, seed=1003)
 CE = dict(T=8192, h=1536, v_pad=51200, v_valid=50257, t=8, seed=1002)
+CE_8P3B = dict(T=4096, h=3072, v_pad=51200, v_valid=50257, t=8, seed=1006)
+SUSTAINED_S = 4.0     # seconds of back-to-back steps in the sustained leg
+SUSTAINED_CHUNK = 50  # steps between the sustained leg's CUDA events
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS_PER_STEP = 8  # fwd: 2, bwd: 4, CE: 2
 KERNEL_SOURCES = ("mptp_gemm.cuh", "mptp_ptx.cuh", "mptp_launch.cuh", "mptp_ce.cu")
@@ -65,21 +74,21 @@ BF16_FLOP_PER_CLK_PER_SM = 8192
 
 
 def peak_table(value, mlp_tf, ce_tf, peaks, peak_src, dev, clocks):
-    """Fractions of the three denominators: the theoretical dense bf16 peak (SMs x per-SM
-    rate x the maximum SM clock seen by nvidia-smi, else the device's), and the measured
-    burst and sustained bf16 GEMM rates."""
+    """Fractions of three denominators, as [step, MLP fwd+bwd, CE]: the theoretical dense bf16
+    peak (SMs x per-SM rate x the SM clock: the maximum nvidia-smi reports, and the median it
+    sampled during the timed steps), and the measured burst and sustained bf16 GEMM rates."""
     import torch
     props = torch.cuda.get_device_properties(dev)
     mhz = (clocks or {}).get("sm_max_mhz")
     if not mhz:
         mhz = getattr(props, "clock_rate", 0) / 1000.0 or 2070.0
-    theo = props.multi_processor_count * BF16_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12
-    out = {"theoretical_dense_bf16": {"tflops": theo, "sms": props.multi_processor_count,
-                                      "flop_per_clk_per_sm": BF16_FLOP_PER_CLK_PER_SM, "clock_mhz": mhz}}
-    for name, key in (("measured_burst", "bf16_tflops"), ("measured_sustained", "bf16_tflops_sustained")):
-        out[name] = {"tflops": peaks[key], "source": peak_src}
-    for d in out.values():
-        d["frac"] = {"step": value / d["tflops"], "mlp_fwd_bwd": mlp_tf / d["tflops"], "ce": ce_tf / d["tflops"]}
+    med = (clocks or {}).get("sm_mhz") or mhz
+    den = {"theoretical_max_clock": theoretical_tflops(dev, mhz), "theoretical_sampled_clock": theoretical_tflops(dev, med),
+           "measured_burst": peaks["bf16_tflops"], "measured_sustained": peaks["bf16_tflops_sustained"]}
+    out = {"tflops": den, "clock_mhz": {"max": mhz, "sampled_median": med}, "source": peak_src,
+           "rate": f"{props.multi_processor_count} SMs x {BF16_FLOP_PER_CLK_PER_SM} FLOP/clk",
+           "order": ["step", "mlp_fwd_bwd", "ce"]}
+    out["frac"] = {k: [value / d, mlp_tf / d, ce_tf / d] for k, d in den.items()}
     return out
 
 
@@ -108,10 +117,10 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary,
-    or None when the kernel sources changed since those counters were taken."""
-    path = os.path.join(ROOT, "profiles", "ce_logits_lse_ncu.txt")
+def profiled_traffic(name="ce_logits_lse_ncu.txt"):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, or None when
+    the kernel sources changed since those counters were taken."""
+    path = os.path.join(ROOT, "profiles", name)
     try:
         with open(path) as fh:
             kv = dict(line.split(":", 1) for line in fh if ":" in line and not line.startswith("#"))
@@ -169,15 +178,19 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, timestamps: bool = False, period_ms: int = 50):
         self.gpu = gpu_index
         self.proc = None
+        self.ts = timestamps
+        self.period = period_ms
+        self.text = ""
 
     def start(self):
+        fields = ("timestamp," if self.ts else "") + self.FIELDS
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={fields}", "--format=csv,noheader,nounits",
+                 "-lms", str(self.period)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
         time.sleep(0.3)
@@ -191,19 +204,34 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        return summarize_clocks(out)
+        self.text = out
+        return summarize_clocks(out, timestamps=self.ts)
 
 
-def summarize_clocks(text: str):
+def parse_clock_rows(text: str, timestamps: bool = False):
+    """(time or None, sm MHz, max MHz, watts, hw_slowdown, hw_thermal, sw_thermal, sw_power_cap) per
+    nvidia-smi sample; `time` is the sample's wall-clock time (epoch seconds) when the query
+    led with the timestamp field."""
+    import datetime
     rows = []
+    off = 1 if timestamps else 0
     for r in csv.reader(io.StringIO(text)):
         r = [x.strip() for x in r]
-        if len(r) < 9:
+        if len(r) < 9 + off:
             continue
         try:
-            rows.append((float(r[1]), float(r[2]), float(r[3]), r[5], r[6], r[7], r[8]))
+            ts = None
+            if timestamps:
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            q = r[off:]
+            rows.append((ts, float(q[1]), float(q[2]), float(q[3]), q[5], q[6], q[7], q[8]))
         except ValueError:
             continue
+    return rows
+
+
+def summarize_clocks(text: str, timestamps: bool = False):
+    rows = [x[1:] for x in parse_clock_rows(text, timestamps)]
     if not rows:
         return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
     loaded = [x for x in rows if x[2] > 300.0] or rows  # samples drawing real power
@@ -325,6 +353,135 @@ def time_breakdown(step, reps, flush):
     return {name: round(event_median(fn, reps, flush), 4) for name, fn in calls.items()}
 
 
+def theoretical_tflops(dev, mhz):
+    """Dense bf16 tensor peak at `mhz`: SMs x per-SM rate x clock."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    return props.multi_processor_count * BF16_FLOP_PER_CLK_PER_SM * mhz * 1e6 / 1e12
+
+
+def bin_chunks_by_clock(chunk_windows, chunk_ms, chunk_flop, rows, bin_mhz=60.0):
+    """Chunks of back-to-back steps binned by the SM clock they ran at.
+
+    chunk_windows: (start, end) wall-clock seconds of each chunk; chunk_ms: its device time;
+    rows: parsed nvidia-smi samples (time first). A chunk's clock is the median of the samples
+    inside its window (chunks with none are left out). Returns one entry per clock bin, lowest
+    first: the bin's centre, the chunks in it, their TFLOP/s and mean clock."""
+    bins = {}
+    for (a, b), ms in zip(chunk_windows, chunk_ms):
+        mhz = sorted(x[1] for x in rows if x[0] is not None and a <= x[0] <= b and x[3] > 300.0)
+        if not mhz or ms <= 0:
+            continue
+        c = mhz[len(mhz) // 2]
+        k = round(c / bin_mhz) * bin_mhz
+        e = bins.setdefault(k, {"ms": 0.0, "n": 0, "mhz": 0.0})
+        e["ms"] += ms
+        e["n"] += 1
+        e["mhz"] += c
+    return [{"mhz_bin": k, "chunks": e["n"], "mean_mhz": e["mhz"] / e["n"],
+             "tflops": chunk_flop * e["n"] / (e["ms"] * 1e-3) / 1e12} for k, e in sorted(bins.items())]
+
+
+def time_sustained(step, dev, gpu, seconds=SUSTAINED_S, chunk=SUSTAINED_CHUNK):
+    """The step back to back for about `seconds` (no flush between steps, as in a training
+    loop), long enough for the power cap to set the clock. CUDA events every `chunk` steps;
+    the clock sampler's timestamps put each chunk at the clock it ran at."""
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(10):
+        step.run()
+    b.record()
+    torch.cuda.synchronize()
+    per_step = max(a.elapsed_time(b) / 10, 1e-3)
+    n_chunks = max(4, int(seconds * 1e3 / (per_step * chunk)))
+    sampler = ClockSampler(gpu, timestamps=True, period_ms=20)
+    sampler.start()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_chunks + 1)]
+    torch.cuda.synchronize()
+    t0 = time.time()
+    evs[0].record()
+    for c in range(n_chunks):
+        for _ in range(chunk):
+            step.run()
+        evs[c + 1].record()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    step.check_status()
+    ends = [evs[0].elapsed_time(e) for e in evs]
+    chunk_ms = [ends[i + 1] - ends[i] for i in range(n_chunks)]
+    windows = [(t0 + ends[i] * 1e-3, t0 + ends[i + 1] * 1e-3) for i in range(n_chunks)]
+    rows = parse_clock_rows(sampler.text, timestamps=True)
+    total_ms = ends[-1]
+    steps = n_chunks * chunk
+    ms_step = total_ms / steps
+    tflops = step_flop() / (ms_step * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    mhz = clocks.get("sm_mhz")
+    out = {"steps": steps, "seconds": total_ms * 1e-3, "ms_per_step": ms_step, "tflops": tflops,
+           "peak": peaks["bf16_tflops_sustained"], "peak_source": f"{peak_src} bf16 sustained",
+           "frac": tflops / peaks["bf16_tflops_sustained"],
+           "clocks": {k: clocks.get(k) for k in ("sm_mhz", "sm_max_mhz", "reasons", "samples", "power_w_max")},
+           "by_clock": bin_chunks_by_clock(windows, chunk_ms, step_flop() * chunk, rows)}
+    if mhz:
+        theo = theoretical_tflops(dev, mhz)
+        out["kcycles_per_step"] = ms_step * mhz  # time x median clock (ms x MHz = 1e3 cycles)
+        out["theoretical_at_median_mhz"] = theo
+        out["frac_of_theoretical_at_median_mhz"] = tflops / theo
+    return out
+
+
+def time_ce_8p3b(dev, reps, flush):
+    """The fused cross-entropy at the 8.3B-layer width (T = 4096 = b 4 x s 1024, h = 3072,
+    vocabulary 50,257 padded to 51,200, t = 8): the logit kernel (K6) alone, the whole call,
+    and K6 against the burst bf16 peak (a kernel timed alone)."""
+    import torch
+
+    import synth
+    import tensor_transformer_layer_gb300 as mp
+    c = CE_8P3B
+    ci = synth.ce_inputs(c["T"], c["h"], c["v_pad"], c["v_valid"], c["seed"])
+    X, E, tg = ci["X"].to(dev), ci["E"].to(dev), ci["target"].to(dev)
+    ws = torch.empty(mp.mp_vocab_ce_workspace_bytes(c["T"], c["v_pad"], c["t"]), dtype=torch.uint8, device=dev)
+    loss = torch.empty(c["T"], dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    part = lambda: mp.mp_vocab_ce_partials(X, E, tg, ws, v_valid=c["v_valid"], t=c["t"], d_status=st)
+    full = lambda: mp.mp_vocab_ce(X, E, tg, loss, ws, v_valid=c["v_valid"], t=c["t"], d_status=st)
+    for _ in range(3):
+        full()
+    k6_ms = event_median(part, reps, flush)
+    ce_ms = event_median(full, reps, flush)
+    torch.cuda.synchronize()
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {int(st.item())} in the 8.3B-layer cross-entropy")
+    flop = 2.0 * c["T"] * c["h"] * c["v_pad"]
+    peaks, peak_src = load_peaks()
+    k6 = flop / (k6_ms * 1e-3) / 1e12
+    out = {"T": c["T"], "h": c["h"], "v_pad": c["v_pad"], "v_valid": c["v_valid"], "t": c["t"],
+           "ms": ce_ms, "tokens_per_s": c["T"] / (ce_ms * 1e-3), "tflops": flop / (ce_ms * 1e-3) / 1e12,
+           "roofline": {"kernel": "K6 mp_vocab_ce_partials", "bound": "tensor", "achieved": k6,
+                        "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": k6 / peaks["bf16_tflops"],
+                        "peak_source": f"{peak_src} bf16 burst (kernel timed alone, L2 flushed, median of {reps})",
+                        "traffic": profiled_traffic("ce_logits_lse_8p3b_ncu.txt"), "flop_per_launch": flop,
+                        "avg_launch_ms": k6_ms}}
+    del X, E, tg, ws, loss
+    torch.cuda.empty_cache()
+    return out
+
+
+def rounded(obj, sig=5):
+    """The same structure with floats rounded to `sig` significant digits (a shorter line)."""
+    if isinstance(obj, float):
+        if obj != obj or obj in (float("inf"), float("-inf")) or obj == 0.0:
+            return obj
+        return float(f"{obj:.{sig}g}")
+    if isinstance(obj, dict):
+        return {k: rounded(v, sig) for k, v in obj.items()}
+    if isinstance(obj, (list, tuple)):
+        return [rounded(v, sig) for v in obj]
+    return obj
+
+
 def combine_row(ms, peaks, peak_src):
     """The step's one memory-bound kernel, the cross-entropy combine (K7), against the measured
     HBM copy bandwidth. Algorithmic bytes: the (max, sum-exp) planes of every partition, one
@@ -334,11 +491,10 @@ def combine_row(ms, peaks, peak_src):
     P = mp.mp_vocab_ce_workspace_bytes(T, CE["v_pad"], CE["t"]) // (12 * T)
     nbytes = 8 * T * P + 12 * T
     gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"kernel": "K7 cross-entropy combine (mp_vocab_ce_combine)", "bound": "hbm", "bytes": nbytes,
+    return {"kernel": "K7 mp_vocab_ce_combine", "bound": "hbm", "bytes": nbytes,
             "partitions": P, "ms": ms, "achieved_gbs": gbs, "peak_gbs": peaks["hbm_gbs"],
             "frac": gbs / peaks["hbm_gbs"], "peak_source": peak_src,
-            "timing": "CUDA events around one call after an L2 flush (launch included); at a few MB the "
-                      "kernel is bound by DRAM latency and the launch, not bandwidth"}
+            "timing": "one call after an L2 flush, launch included: latency-bound at a few MB"}
 
 
 def time_next_rows(step, reps, flush):
@@ -398,15 +554,14 @@ def time_next_rows(step, reps, flush):
     attn_core = 4.0 * ab * aheads * hd * as_ * (as_ + 1) / 2     # QK^T and PV over the causal pairs
     attn_flop = 2.0 * aT * ah * 3 * ah + attn_core + 2.0 * aT * ah * ah
     attn = {"ms": ams, "tflops": attn_flop / (ams * 1e-3) / 1e12, "flop": attn_flop,
-            "shape": {"b": ab, "s": as_, "h": ah, "heads": aheads, "head_dim": hd, "t": at},
-            "flop_note": "QKV 6*T*h^2 + causal attention 4*b*heads*d*s(s+1)/2 + out 2*T*h^2; launches 3"}
+            "shape": [ab, as_, ah, aheads, hd, at],
+            "flop_note": "shape b,s,h,heads,d,t; QKV 6Th^2 + causal 4*b*heads*d*s(s+1)/2 + out 2Th^2"}
     algo = 4.0 * T * h * v_pad      # dX = dZ E and dE = dZ^T X
     executed = 6.0 * T * h * v_pad  # plus the logit recompute (logits are never stored)
     return {"ce_bwd": {"ms": ms, "tflops_algorithmic": algo / (ms * 1e-3) / 1e12,
                        "tflops_executed": executed / (ms * 1e-3) / 1e12, "tokens_per_s": T / (ms * 1e-3),
-                       "workspace": "one pass (every shard's dZ, T*v_pad bf16); launches 4",
-                       "ms_shard_by_shard": ce_ms["shard_by_shard"], "launches_shard_by_shard": 1 + 3 * t,
-                       "flop_note": "algorithmic 4*T*h*v_pad (dX, dE); executed adds the 2*T*h*v_pad recompute"},
+                       "ms_shard_by_shard": ce_ms["shard_by_shard"],
+                       "flop_note": "one-pass workspace; algorithmic 4Thv (dX, dE), executed adds the 2Thv recompute"},
             "vocab_embed": embed,
             "attn_fwd": attn}
 
@@ -439,9 +594,7 @@ def time_torch_context(step, reps, flush):
     torch.cuda.empty_cache()
     return {"mlp_fwd_bwd_ms": mlp_ms, "mlp_tflops": mlp_flop() / (mlp_ms * 1e-3) / 1e12,
             "ce_ms": ce_ms, "ce_tflops": ce_flop() / (ce_ms * 1e-3) / 1e12,
-            "ce_tokens_per_s": CE["T"] / (ce_ms * 1e-3),
-            "note": "PyTorch + cuBLAS composition of the same step (context only): F.gelu(X@A)@B with "
-                    "autograd backward; (X@E^T)[:, :v_valid] in fp32 then F.cross_entropy"}
+            "note": "PyTorch/cuBLAS: F.gelu(X@A)@B + autograd; fp32 (X@E^T)[:, :v_valid] + F.cross_entropy"}
 
 
 # Per-step host traffic of the two end-to-end measurements. "batch": the weights A, B, E are
@@ -605,11 +758,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing (profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer pass (profiling runs)")
     ap.add_argument("--no-next-rows", action="store_true", help="skip the rows measured beside the step")
+    ap.add_argument("--no-sustained", action="store_true", help="skip the seconds-long back-to-back leg")
     ap.add_argument("--no-context", action="store_true",
                     help="skip the PyTorch/cuBLAS composition timed beside the step for context")
     ap.add_argument("--sweep", action="store_true",
                     help="time MLP fwd+bwd and the fused CE at every point of the layer sweep (one JSON line each)")
-    ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "mlp", "attn"), default="none",
+    ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "ce_8p3b", "mlp", "attn"), default="none",
                     help="run only a small case of one entry point a few times (for ncu), print nothing")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.profile_case == "none":
@@ -664,6 +818,7 @@ def main(argv=None):
     ce_achieved = ce_flop() / (ce_avg_ms * 1e-3) / 1e12
     traffic = profiled_traffic()
     mlp_ms = breakdown["mlp_fwd"] + breakdown["mlp_bwd"]
+    ce_call_ms = breakdown["ce_partials"] + breakdown["ce_combine"]
 
     e2e = e2e_all = None
     if not args.no_e2e:
@@ -677,9 +832,10 @@ def main(argv=None):
         all_ms, h2d, d2h = time_e2e(step, max(3, min(args.steps, 30)), 3)
         all_ms = max_over_ranks(all_ms, world, dev)
         e2e_all = {"value": world * step_flop() / (all_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                   "ms_per_step": all_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                   "host_in": list(step.host_in), "host_out": list(step.out_names), "pipeline": pipe}
+                   "ms_per_step": all_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     step.check_status()
+    sustained = None if args.no_sustained else time_sustained(step, dev, physical_gpu(local_rank))
+    ce83 = None if args.no_next_rows else time_ce_8p3b(dev, 9, flush)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -692,33 +848,39 @@ def main(argv=None):
                          f"weights) + {sample.ce_tokens} CE tokens (full embedding) in {el:.1f} s"}
 
     if rank == 0:
+        mlp_tf = mlp_flop() / (mlp_ms * 1e-3) / 1e12
+        ce_tf = ce_flop() / (ce_call_ms * 1e-3) / 1e12
+        theo_sampled = theoretical_tflops(dev, clocks.get("sm_mhz") or clocks.get("sm_max_mhz") or 2070.0)
+        # Contract keys first; the context objects next; the headline sub-metrics last, so that a
+        # reader of only the line's tail still sees them.
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(),
-            "pct_of_measured_bf16_sustained": value / peaks["bf16_tflops_sustained"],
-            "pct_of_peak": peak_table(value, mlp_flop() / (mlp_ms * 1e-3) / 1e12,
-                                      ce_flop() / ((breakdown["ce_partials"] + breakdown["ce_combine"]) * 1e-3) / 1e12,
-                                      peaks, peak_src, dev, clocks),
-            "mlp_fwd_bwd_tflops": mlp_flop() / (mlp_ms * 1e-3) / 1e12,
-            "ce_tokens_per_s": CE["T"] / ((breakdown["ce_partials"] + breakdown["ce_combine"]) * 1e-3),
-            "ce_tflops": ce_flop() / ((breakdown["ce_partials"] + breakdown["ce_combine"]) * 1e-3) / 1e12,
-            "breakdown_ms": breakdown,
-            "next_rows": next_rows,
-            "torch_context": context,
-            "memory_bound": combine_row(breakdown["ce_combine"], peaks, peak_src),
-            "roofline": {"kernel": "mp_vocab_ce_partials (logit GEMM + online LSE epilogue)", "bound": "tensor",
-                         "achieved": ce_achieved, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                         "frac": ce_achieved / peaks["bf16_tflops_sustained"],
-                         "peak_source": f"{peak_src} bf16 sustained", "traffic": traffic,
-                         "algorithmic_flop_per_launch": ce_flop(), "avg_launch_ms": ce_avg_ms},
+            "gpu_launches": KERNELS_PER_STEP * (args.steps),
+            "clocks": clocks,
+            "roofline": {"kernel": "K6 mp_vocab_ce_partials (logit GEMM + online LSE epilogue)", "bound": "tensor",
+                         "achieved": ce_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": ce_achieved / peaks["bf16_tflops"],
+                         "peak_source": f"{peak_src} bf16 burst (timed inside short steps)", "traffic": traffic,
+                         "algorithmic_flop_per_launch": ce_flop(), "avg_launch_ms": ce_avg_ms,
+                         "theoretical_at_sampled_clock": theo_sampled,
+                         "frac_of_theoretical_at_sampled_clock": ce_achieved / theo_sampled},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "e2e_all_tensors": e2e_all,
-            "gpu_launches": KERNELS_PER_STEP * (args.steps),
-            "clocks": clocks,
+            "torch_context": context,
+            "memory_bound": combine_row(breakdown["ce_combine"], peaks, peak_src),
+            "next_rows": next_rows,
+            "pct_of_peak": peak_table(value, mlp_tf, ce_tf, peaks, peak_src, dev, clocks),
+            "breakdown_ms": breakdown,
+            "ce_8p3b": ce83,
+            "sustained": sustained,
+            "mlp_fwd_bwd_tflops": mlp_tf,
+            "ce_tflops": ce_tf,
+            "ce_tokens_per_s": CE["T"] / (ce_call_ms * 1e-3),
         }
-        print(json.dumps(line), flush=True)
+        print(json.dumps(rounded(line)), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
@@ -771,9 +933,9 @@ def run_sweep(dev, reps, warmup):
 
 
 def profile_case(which, dev):
-    """Cases for ncu captures: 'ce' (T=2048) and 'mlp' (the 8.3B layer, 0.7 GB) are small enough for
-    multi-pass captures (under 1 GB on the device, 0.2-0.7 ms kernels, inputs > L2); 'ce_full' is the
-    bench's CE launch, for one-pass metrics only."""
+    """Cases for ncu captures: 'ce' (T=2048), 'ce_8p3b' (T=4096, h=3072: 0.35 GB) and 'mlp' (the 8.3B
+    layer, 0.7 GB) are small enough for multi-pass captures (under 1 GB on the device, 0.2-0.7 ms
+    kernels, inputs > L2); 'ce_full' is the bench's CE launch, for one-pass metrics only."""
     import torch
 
     import synth
@@ -789,9 +951,12 @@ def profile_case(which, dev):
             mp.mp_attn_fwd(X, Wqkv, Wo, out, QKV, O, b=b, s=s_, heads=heads, t=t)
         torch.cuda.synchronize()
         return 0
-    if which in ("ce", "ce_full"):
+    if which in ("ce", "ce_full", "ce_8p3b"):
         T, h, v_pad, v_valid, t = (2048 if which == "ce" else CE["T"]), 1536, 51200, 50257, 8
-        ci = synth.ce_inputs(T, h, v_pad, v_valid, seed=1002)
+        seed = 1002
+        if which == "ce_8p3b":
+            T, h, seed = CE_8P3B["T"], CE_8P3B["h"], CE_8P3B["seed"]
+        ci = synth.ce_inputs(T, h, v_pad, v_valid, seed=seed)
         X, E, tgt = ci["X"].to(dev), ci["E"].to(dev), ci["target"].to(dev)
         ws = torch.empty(mp.mp_vocab_ce_workspace_bytes(T, v_pad, t), dtype=torch.uint8, device=dev)
         loss = torch.empty(T, dtype=torch.float32, device=dev)

@@ -84,5 +84,6 @@ WORKLOADS = {
     "mlp_1p2b": dict(T=8192, h=1536, f=6144, t=(2, 4), seed=1001),
     "ce_1p2b": dict(T=8192, h=1536, v_pad=51200, v_valid=50257, t=8, seed=1002),
     "mlp_8p3b": dict(T=4096, h=3072, f=12288, t=8, seed=1003),
+    "ce_8p3b": dict(T=4096, h=3072, v_pad=51200, v_valid=50257, t=8, seed=1006),
     "sweep": dict(h=(1536, 1920, 2304, 3072), T=(2048, 8192), t=(1, 2, 4, 8), v_pad=51200, v_valid=50257, seed=1004),
 }

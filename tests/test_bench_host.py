@@ -90,3 +90,29 @@ def test_combine_row_bytes():
     assert row["bytes"] == 8 * P * T + 12 * T and row["partitions"] == P
     assert abs(row["achieved_gbs"] - row["bytes"] / 1e-5 / 1e9) < 1e-6
     assert abs(row["frac"] - row["achieved_gbs"] / 5000.0) < 1e-12 and row["bound"] == "hbm"
+
+
+def test_clock_rows_with_timestamps_and_binning():
+    import datetime
+    base = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    lines = []
+    for i, mhz in enumerate((1600, 1610, 1900, 1905, 1898)):
+        ts = (base + datetime.timedelta(milliseconds=100 * i)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        lines.append(f"{ts}, 0, {mhz}, 2070, 1200.0, 0x4, Not Active, Not Active, Not Active, Active")
+    text = "\n".join(lines) + "\n"
+    rows = bench.parse_clock_rows(text, timestamps=True)
+    assert len(rows) == 5 and rows[0][1] == 1600.0 and rows[1][0] - rows[0][0] == pytest.approx(0.1, abs=1e-6)
+    c = bench.summarize_clocks(text, timestamps=True)
+    assert c["samples"] == 5 and c["reasons"] == ["sw_power_cap"] and c["sm_mhz"] == 1898.0
+    t0 = rows[0][0]
+    # chunk 0 covers the two 1.6 GHz samples, chunk 1 the three 1.9 GHz ones, chunk 2 no sample
+    windows = [(t0 - 0.01, t0 + 0.15), (t0 + 0.15, t0 + 0.45), (t0 + 1.0, t0 + 2.0)]
+    bins = bench.bin_chunks_by_clock(windows, [2.0, 1.0, 1.0], 1e12, rows, bin_mhz=60.0)
+    assert [b["chunks"] for b in bins] == [1, 1]
+    assert bins[0]["mhz_bin"] == 1620.0 and bins[1]["mhz_bin"] == 1920.0
+    assert bins[0]["tflops"] == pytest.approx(1e12 / 2e-3 / 1e12) and bins[1]["tflops"] == pytest.approx(1000.0)
+
+
+def test_rounded_keeps_structure():
+    v = bench.rounded({"a": 1.23456789, "b": [2.0000001, None, "x"], "c": {"d": float("nan"), "e": 0.0}}, 4)
+    assert v["a"] == 1.235 and v["b"] == [2.0, None, "x"] and v["c"]["e"] == 0.0 and v["c"]["d"] != v["c"]["d"]

@@ -39,6 +39,19 @@ def test_ce_1p2b_vocab_sampled():
     assert np.all(np.isfinite(got))
 
 
+def test_ce_8p3b_layer_sampled():
+    # The 8.3B-layer width: T = 4096 (b = 4, s = 1024), h = 3072, the same vocabulary and
+    # t = 8, in the launch configuration the bench times; sampled tokens incl. the last.
+    w = synth.WORKLOADS["ce_8p3b"]
+    inp = synth.ce_inputs(w["T"], w["h"], w["v_pad"], w["v_valid"], w["seed"])
+    got = run_ce(inp, w["v_valid"], w["t"])
+    rows = synth.sample_indices(w["T"], 192, seed=22).numpy()
+    want = oracle.ce_loss(f64(inp["X"])[rows], f64(inp["E"]), inp["target"].numpy()[rows], w["v_valid"])
+    err = np.max(np.abs(got[rows] - want))
+    assert err <= LOSS_ABS, err
+    assert np.all(np.isfinite(got))
+
+
 def test_ce_zero_embedding_closed_form():
     inp = synth.ce_inputs(200, 128, 51200, 50257, seed=4100)
     inp["E"] = torch.zeros_like(inp["E"])
