@@ -93,6 +93,14 @@ def test_mlp_fwd_rejects_shapes(L, T, h, f, t, code):
     assert L.mp_mlp_bwd(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, T, h, f, t, None, None) == code
 
 
+@pytest.mark.parametrize("s0,n", [(-1, 1), (0, 0), (1, 2), (2, 1), (0, 3)])
+def test_mlp_shards_reject_bad_ranges(L, s0, n):
+    # t = 2: valid ranges are (0,1), (1,1), (0,2); anything else is MP_ERR_INVALID_ARG before any launch.
+    assert L.mp_mlp_fwd_shards(FAKE, FAKE, FAKE, FAKE, FAKE, None, 8, 64, 128, 2, s0, n, None, None) == 1
+    assert L.mp_mlp_bwd_shards(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 128, 2, s0, n,
+                               None, None) == 1
+
+
 def test_mlp_rejects_null_and_misaligned(L):
     assert L.mp_mlp_fwd(None, FAKE, FAKE, FAKE, FAKE, None, 8, 64, 128, 1, None, None) == 1
     assert L.mp_mlp_fwd(FAKE, FAKE, FAKE, FAKE, None, None, 8, 64, 128, 1, None, None) == 1
@@ -130,6 +138,10 @@ def test_no_device_answer(L):
     # Valid arguments on a machine without a GB300: MP_ERR_NO_DEVICE, nothing launched.
     assert L.mp_mlp_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, 8, 64, 128, 1, None, None) == 4
     assert L.mp_vocab_ce(FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, 4, 64, 256, 200, 1, None, None) == 4
+    # The no-allocation entry point: a T = 0 call also reaches the device (it places the static
+    # array there), so without one it answers MP_ERR_NO_DEVICE; too large a problem is refused first.
+    assert L.mp_vocab_ce_noalloc(None, None, None, None, 0, 64, 256, 200, 1, None, None) == 4
+    assert L.mp_vocab_ce_noalloc(FAKE, FAKE, FAKE, FAKE, 8739, 64, 51200, 50257, 8, None, None) == 8
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

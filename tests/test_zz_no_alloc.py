@@ -3,9 +3,11 @@ allocate device memory (their memory belongs to another pool that forbids
 cudaMalloc/cudaFree after start-up), so they cannot pass a workspace. Its
 scratch is the library's fixed 4 MiB static device array.
 
-Called through the C ABI (ctypes, raw device pointers) twice in a row with
-different inputs, and compared with the workspace-taking mp_vocab_ce at the
-per-token loss tolerance used by the other cross-entropy tests. Collected last
+Called through the C ABI (ctypes, raw device pointers) several times in a row:
+the same small shape twice with new inputs, then the largest shape the array
+holds, then the small shape again. Each result is compared with the
+workspace-taking mp_vocab_ce at the per-token loss tolerance used by the other
+cross-entropy tests, and sampled tokens with the float64 oracle. Collected last
 (file name) so a stop-at-first-failure run has already run everything else.
 """
 import ctypes
@@ -14,8 +16,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
-from gpu_util import LOSS_ABS
+from gpu_util import LOSS_ABS, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -49,19 +52,25 @@ def _noalloc(L, X, E, tgt, v_valid, t):
     return loss.cpu().numpy()
 
 
-def test_noalloc_matches_workspace_entry_point_twice():
+def test_noalloc_matches_workspace_entry_point_and_oracle():
     mp, L = _lib()
-    cases = [
-        dict(T=8192, h=1536, v_pad=51200, v_valid=50257, t=8, seed=5100),   # 3.75 MiB of triples
-        dict(T=300, h=128, v_pad=2048, v_valid=2000, t=4, seed=5101),       # a different partition count
-    ]
-    for c in cases:   # two calls in a row on the shared array
+    # A T = 0 call places the static array on this device (it is what a caller whose pool will
+    # reserve the rest of HBM makes first); it launches nothing.
+    code = L.mp_vocab_ce_noalloc(None, None, None, None, 0, 128, 2048, 2000, 4, None, None)
+    assert code == 0, code
+    small = dict(T=300, h=128, v_pad=2048, v_valid=2000, t=4)
+    large = dict(T=8192, h=1536, v_pad=51200, v_valid=50257, t=8)   # 3.75 MiB of triples
+    cases = [dict(small, seed=5101), dict(small, seed=5102), dict(large, seed=5100), dict(small, seed=5103)]
+    for c in cases:   # calls in a row on the shared array, which keeps the previous call's triples
         inp = synth.ce_inputs(c["T"], c["h"], c["v_pad"], c["v_valid"], c["seed"])
         X, E, tgt = inp["X"].cuda(), inp["E"].cuda(), inp["target"].cuda()
         want = _existing(mp, X, E, tgt, c["v_valid"], c["t"])
         got = _noalloc(L, X, E, tgt, c["v_valid"], c["t"])
         assert np.all(np.isfinite(got))
-        assert float(np.max(np.abs(got.astype(np.float64) - want))) <= LOSS_ABS
+        assert float(np.max(np.abs(got.astype(np.float64) - want))) <= LOSS_ABS, c
+        rows = synth.sample_indices(c["T"], 32, seed=c["seed"]).numpy()
+        ref = oracle.ce_loss(f64(inp["X"])[rows], f64(inp["E"]), inp["target"].numpy()[rows], c["v_valid"])
+        assert float(np.max(np.abs(got[rows].astype(np.float64) - ref))) <= LOSS_ABS, c
 
 
 def test_noalloc_refuses_problems_beyond_the_array():
