@@ -22,8 +22,10 @@
  *   - All matrices are bf16 (raw bits in mp_bf16), row-major and contiguous,
  *     except targets (int32), loss (fp32) and workspaces (opaque bytes).
  *   - All pointers are DEVICE pointers, 16-byte aligned. The caller allocates,
- *     owns and frees every buffer; the library keeps no device memory between
- *     calls and never allocates.
+ *     owns and frees every buffer; the library never allocates and keeps no
+ *     device memory between calls, with one exception: the static 4 MiB array
+ *     of mp_vocab_ce_noalloc, which a device holds from that entry point's
+ *     first call on it until the process exits.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Calls only enqueue work on it and return; nothing synchronises the host.
  *   - Argument and shape errors are reported synchronously, before any launch
@@ -125,6 +127,41 @@ MP_API mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B
                      mp_bf16* dX, mp_bf16* dA, mp_bf16* dB, mp_bf16* dU_ws,
                      int T, int h, int f, int t,
                      uint32_t* d_status, void* stream);
+
+/*
+ * The same two computations for a range of shards [shard_begin, shard_begin +
+ * shard_count) of the t shards: the work the GPUs holding those shards do before
+ * the all-reduce ("Megatron-LM: Training Multi-Billion Parameter Language Models
+ * Using Model Parallelism", section 3.4 "Row-Parallel GEMM for the Second MLP
+ * Layer": each GPU's partial output, summed by g; "Megatron-LM, annotated",
+ * section 3.1, "The second matrix: cut by rows, add once", which prints the two
+ * partials of its one-token example). With c = [shard_begin f/t, (shard_begin +
+ * shard_count) f/t):
+ *   mp_mlp_fwd_shards:  Y[:, c] = GeLU(X A[:, c]) (and U_save[:, c]);
+ *                       Z = sum over the range's shards i, ascending, of Y_i B_i
+ *                       (the partial output; the full sum when the range is [0, t)).
+ *   mp_mlp_bwd_shards:  dU_ws[:, c] = (dZ B[c, :]^T) * GeLU'(U[:, c]);
+ *                       dX = sum over the range's shards i of dU_i A_i^T (the part
+ *                       of dX those shards give before the f all-reduce);
+ *                       dA[:, c] = X^T dU_ws[:, c];  dB[c, :] = Y[:, c]^T dZ.
+ * Tensors are the full-size ones of mp_mlp_fwd / mp_mlp_bwd (shard i is a view);
+ * only the range's columns of Y, U_save, dU_ws, dA and rows of dB are written, the
+ * rest is left untouched. Each of those elements equals the full call's bit for
+ * bit. Size rules as mp_mlp_fwd, and 0 <= shard_begin, 1 <= shard_count,
+ * shard_begin + shard_count <= t (else MP_ERR_INVALID_ARG). mp_mlp_fwd and
+ * mp_mlp_bwd are these calls with the range [0, t). A device that holds only its
+ * own shards, contiguously, gets its partial from mp_mlp_fwd / mp_mlp_bwd with its
+ * local f and t.
+ */
+MP_API mp_status mp_mlp_fwd_shards(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B,
+                            mp_bf16* Z, mp_bf16* Y, mp_bf16* U_save,
+                            int T, int h, int f, int t, int shard_begin, int shard_count,
+                            uint32_t* d_status, void* stream);
+MP_API mp_status mp_mlp_bwd_shards(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B,
+                            const mp_bf16* U, const mp_bf16* Y, const mp_bf16* dZ,
+                            mp_bf16* dX, mp_bf16* dA, mp_bf16* dB, mp_bf16* dU_ws,
+                            int T, int h, int f, int t, int shard_begin, int shard_count,
+                            uint32_t* d_status, void* stream);
 
 /*
  * Bytes of workspace mp_vocab_ce needs: fp32 triples [P][3][T], P = the number
@@ -243,16 +280,25 @@ MP_API mp_status mp_attn_fwd(const mp_bf16* X, const mp_bf16* Wqkv, const mp_bf1
  *
  * Same inputs, outputs and size rules as mp_vocab_ce, without the workspace: the
  * triples live in a static device array of MP_CE_NOALLOC_MAX_FLOATS floats
- * (4 MiB) that the library reserves on every GPU that loads it, until exit.
+ * (4 MiB), held by every GPU the entry point has run on, until exit.
  *   - Problems needing more than that (mp_vocab_ce_workspace_bytes(T, v_pad, t)
  *     > 4 MiB, e.g. T > 8738 at v_pad = 51,200, t = 8) return MP_ERR_WORKSPACE
  *     before any launch.
- *   - Nothing is allocated: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on a device looks up the array's device address with that
- *     device current; make that first call before any stream capture.
+ *   - Nothing is allocated by the call: no cudaMalloc, cudaFree or allocating
+ *     library call. CUDA itself places the array on a device when it loads the
+ *     code that holds it, which with lazy module loading (the default) is this
+ *     entry point's first call on that device, T = 0 included. Make one call
+ *     (T = 0 suffices) with the device current before a memory pool reserves
+ *     the rest of HBM and before any stream capture, or run the process with
+ *     CUDA_MODULE_LOADING=EAGER.
+ *   - Every call looks up the array's device address with the current device
+ *     (a host-side query), so it stays valid after cudaDeviceReset.
  *   - Every call on a device shares the one array, which keeps the last call's
  *     contents (nothing in it needs to start at zero). Calls whose work overlaps
  *     on the GPU (other streams, other host threads) race on it: serialise them.
+ *   - If the logit kernel gives up on a bounded wait it writes no triples, and
+ *     the losses may then be computed from the previous call's triples: they can
+ *     look valid. Pass d_status and check it for MP_DEV_TIMEOUT.
  */
 #define MP_CE_NOALLOC_MAX_FLOATS (1024 * 1024)
 MP_API mp_status mp_vocab_ce_noalloc(const mp_bf16* X, const mp_bf16* E, const int32_t* target,

@@ -9,6 +9,7 @@ missing or fails to load, calls raise.
 Shapes (row-major, contiguous):
   mp_mlp_fwd(X[T,h], A[h,f], B[f,h], Z[T,h], Y[T,f], U_save[T,f] | None, t)
   mp_mlp_bwd(X, A, B, U[T,f], Y[T,f], dZ[T,h], dX[T,h], dA[h,f], dB[f,h], dU_ws[T,f], t)
+  mp_mlp_fwd_shards / mp_mlp_bwd_shards: the same with shard_begin, shard_count
   mp_vocab_ce(X[T,h], E[v_pad,h], target[T] int32, loss[T] fp32, workspace uint8, v_valid, t)
 """
 from __future__ import annotations
@@ -30,7 +31,7 @@ STATUS_NAMES = {
     8: "MP_ERR_WORKSPACE",
 }
 # Every symbol include/mptp.h declares.
-EXPORTS = ("mp_mlp_fwd", "mp_mlp_bwd", "mp_vocab_ce_workspace_bytes", "mp_vocab_ce", "mp_vocab_ce_partials",
+EXPORTS = ("mp_mlp_fwd", "mp_mlp_bwd", "mp_mlp_fwd_shards", "mp_mlp_bwd_shards", "mp_vocab_ce_workspace_bytes", "mp_vocab_ce", "mp_vocab_ce_partials",
            "mp_vocab_ce_combine", "mp_status_string", "mp_status_from_device", "mp_version",
            "mp_vocab_ce_noalloc", "mp_vocab_ce_bwd_workspace_bytes", "mp_vocab_ce_bwd_workspace_bytes_one_pass",
            "mp_vocab_ce_bwd", "mp_vocab_embed",
@@ -60,6 +61,10 @@ def lib() -> ctypes.CDLL:
         L.mp_mlp_fwd.restype = _I
         L.mp_mlp_bwd.argtypes = [_P] * 10 + [_I, _I, _I, _I, _P, _P]
         L.mp_mlp_bwd.restype = _I
+        L.mp_mlp_fwd_shards.argtypes = [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]
+        L.mp_mlp_fwd_shards.restype = _I
+        L.mp_mlp_bwd_shards.argtypes = [_P] * 10 + [_I, _I, _I, _I, _I, _I, _P, _P]
+        L.mp_mlp_bwd_shards.restype = _I
         L.mp_vocab_ce_workspace_bytes.argtypes = [_I, _I, _I]
         L.mp_vocab_ce_workspace_bytes.restype = ctypes.c_size_t
         L.mp_vocab_ce.argtypes = [_P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P, _P]
@@ -156,6 +161,35 @@ def mp_mlp_bwd(X, A, B, U, Y, dZ, dX, dA, dB, dU_ws, *, t: int, d_status=None, s
         _ptr(dX, "dX", shape=(T, h)), _ptr(dA, "dA", shape=(h, f)), _ptr(dB, "dB", shape=(f, h)),
         _ptr(dU_ws, "dU_ws", shape=(T, f)), T, h, f, int(t), _status_ptr(d_status), _stream(stream))
     _check("mp_mlp_bwd", code)
+
+
+def mp_mlp_fwd_shards(X, A, B, Z, Y, U_save=None, *, t: int, shard_begin: int, shard_count: int, d_status=None,
+                      stream=None) -> None:
+    """Forward of shards [shard_begin, shard_begin + shard_count): their columns of Y (and
+    U_save) and their partial output Z = sum over the range of Y_i B_i."""
+    T, h = X.shape
+    f = A.shape[1]
+    code = lib().mp_mlp_fwd_shards(
+        _ptr(X, "X", shape=(T, h)), _ptr(A, "A", shape=(h, f)), _ptr(B, "B", shape=(f, h)),
+        _ptr(Z, "Z", shape=(T, h)), _ptr(Y, "Y", shape=(T, f)),
+        _ptr(U_save, "U_save", shape=(T, f), allow_none=True),
+        T, h, f, int(t), int(shard_begin), int(shard_count), _status_ptr(d_status), _stream(stream))
+    _check("mp_mlp_fwd_shards", code)
+
+
+def mp_mlp_bwd_shards(X, A, B, U, Y, dZ, dX, dA, dB, dU_ws, *, t: int, shard_begin: int, shard_count: int,
+                      d_status=None, stream=None) -> None:
+    """Backward of shards [shard_begin, shard_begin + shard_count): their part of dX, their
+    columns of dA and dU_ws, their rows of dB."""
+    T, h = X.shape
+    f = A.shape[1]
+    code = lib().mp_mlp_bwd_shards(
+        _ptr(X, "X", shape=(T, h)), _ptr(A, "A", shape=(h, f)), _ptr(B, "B", shape=(f, h)),
+        _ptr(U, "U", shape=(T, f)), _ptr(Y, "Y", shape=(T, f)), _ptr(dZ, "dZ", shape=(T, h)),
+        _ptr(dX, "dX", shape=(T, h)), _ptr(dA, "dA", shape=(h, f)), _ptr(dB, "dB", shape=(f, h)),
+        _ptr(dU_ws, "dU_ws", shape=(T, f)), T, h, f, int(t), int(shard_begin), int(shard_count),
+        _status_ptr(d_status), _stream(stream))
+    _check("mp_mlp_bwd_shards", code)
 
 
 def mp_vocab_ce_workspace_bytes(T: int, v_pad: int, t: int) -> int:

@@ -16,6 +16,13 @@
 // the f sum of dX is inside K4's K-loop, and the overlap becomes K4, K5a and K5b side
 // by side on disjoint sets of CTA pairs (the caller's stream plus two side streams),
 // so that none of them ends in a part-empty last wave of tiles.
+//
+// Shard ranges. mp_mlp_fwd_shards / mp_mlp_bwd_shards run the work of shards
+// [s0, s0 + n) only: K1, K3 and K5 over the range's f/t-wide column (or row) blocks,
+// K2 and K4 over the range's K blocks, so Z (dX) is the partial output those shards
+// contribute before the g (f) all-reduce. mp_mlp_fwd and mp_mlp_bwd are the full
+// range [0, t). Every output element runs the same K-loop whichever range it is
+// computed in, so a range's Y, U, dU, dA and dB blocks equal the full call's bitwise.
 #include <cstdlib>
 #include <cstring>
 
@@ -27,6 +34,11 @@ namespace mptp {
 static mp_status check_mlp_shape(int T, int h, int f, int t) {
     if (T < 0 || h <= 0 || f <= 0 || t < 1) return MP_ERR_INVALID_ARG;
     if (h % 64 != 0 || f % t != 0 || (f / t) % 64 != 0) return MP_ERR_UNSUPPORTED_SHAPE;
+    return MP_OK;
+}
+
+static mp_status check_shard_range(int t, int s0, int n) {
+    if (s0 < 0 || n < 1 || s0 > t - n) return MP_ERR_INVALID_ARG;
     return MP_OK;
 }
 
@@ -63,30 +75,13 @@ static BwdSchedule bwd_schedule() {
 // Cost of one output tile in K-block times: its K blocks plus about two for the epilogue.
 constexpr int EPI_KB = 2;
 
-// Epilogues: bf16 rows staged in shared memory and written by TMA stores (whole lines). The
-// register-store forms (EPI_*_G: 16-byte pieces of 32 rows per store instruction, and a seventh
-// pipeline stage) finish a lone launch as fast, but 200 back-to-back steps at the power cap ran
-// 1.3% slower with them: the partial-line writes cost clock.
-#ifndef MPTP_STORE_EPI
-#define MPTP_STORE_EPI EPI_STORE
-#endif
-#ifndef MPTP_GELU_EPI
-#define MPTP_GELU_EPI EPI_GELU
-#endif
-#ifndef MPTP_DGELU_EPI
-#define MPTP_DGELU_EPI EPI_DGELU
-#endif
-// Epilogue warps of K1 and K3.
-#ifndef MPTP_K13_NE
-#define MPTP_K13_NE 4
-#endif
+// Epilogue warps of K1 and K3 (four measured 0.2-0.8 % faster than eight).
+constexpr int K13_NE = 4;
 
 // Tile width of K4 (dX = dU A^T, N = h, B operand K-major). 224-wide tiles cut h = 3072
 // into 14 column units instead of 12, so T = 4096 gives 224 units: 2.95 rounds of 76 CTA
 // pairs, against 2.53 rounds of 256-wide tiles whose last round leaves half the pairs idle.
-#ifndef MPTP_K4_BN
-#define MPTP_K4_BN 224
-#endif
+constexpr int K4_BN = 224;
 
 static GemmArgs launch_args(uint32_t* status) {
     GemmArgs a{};
@@ -100,10 +95,12 @@ static GemmArgs launch_args(uint32_t* status) {
 
 using namespace mptp;
 
-extern "C" mp_status mp_mlp_fwd(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B, mp_bf16* Z, mp_bf16* Y,
-                                mp_bf16* U_save, int T, int h, int f, int t, uint32_t* d_status, void* stream) {
+extern "C" mp_status mp_mlp_fwd_shards(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B, mp_bf16* Z,
+                                       mp_bf16* Y, mp_bf16* U_save, int T, int h, int f, int t, int shard_begin,
+                                       int shard_count, uint32_t* d_status, void* stream) {
     mp_status st = check_mlp_shape(T, h, f, t);
     if (st != MP_OK) return st;
+    if ((st = check_shard_range(t, shard_begin, shard_count)) != MP_OK) return st;
     if (T == 0) return MP_OK;
     if (!X || !A || !B || !Z || !Y) return MP_ERR_INVALID_ARG;
     if (!aligned16(X) || !aligned16(A) || !aligned16(B) || !aligned16(Z) || !aligned16(Y) ||
@@ -113,46 +110,50 @@ extern "C" mp_status mp_mlp_fwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
     if ((st = check_device(&sms)) != MP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const double Tb = 2.0 * T, hb = 2.0 * h;
+    // The range's columns of A, Y and U: [c0, c0 + nc), whole 64-wide blocks (f/t % 64 == 0).
+    const int fs = f / t;
+    const int c0 = shard_begin * fs, nc = shard_count * fs;
 
-    // K1: column-parallel GEMM + GeLU over all shards' columns: U = X A (A MN-major), Y = GeLU(U).
+    // K1: column-parallel GEMM + GeLU over the range's columns: U = X A_r (A MN-major), Y = GeLU(U).
     TmapSet m1{};
     int b1 = 0;
-    if (!make_tmap_bf16(&m1.a, X, h, T, h, 64, BM) || !(b1 = make_tmap_mn_operand(&m1.b, A, f, h, f)) ||
-        !make_tmap_bf16_out(&m1.o0, Y, f, T, f) ||
-        (U_save && !make_tmap_bf16_out(&m1.o1, U_save, f, T, f)))
+    if (!make_tmap_bf16(&m1.a, X, h, T, h, 64, BM) || !(b1 = make_tmap_mn_operand(&m1.b, A + c0, nc, h, f)) ||
+        !make_tmap_bf16_out(&m1.o0, Y + c0, nc, T, f) ||
+        (U_save && !make_tmap_bf16_out(&m1.o1, U_save + c0, nc, T, f)))
         return MP_ERR_CUDA;
     GemmArgs a1 = launch_args(d_status);
-    a1.pr = problem(T, f, 256, 0, h / BK, false, true, Tb * h, hb * f);
+    a1.pr = problem(T, nc, 256, 0, h / BK, false, true, Tb * h, hb * nc);
     a1.pr.b_mn = b1;
     a1.has_out1 = U_save ? 1 : 0;
-    a1.out0 = reinterpret_cast<__nv_bfloat16*>(Y);
-    a1.ld_out0 = f;
-    a1.out1 = reinterpret_cast<__nv_bfloat16*>(U_save);
-    a1.ld_out1 = f;
-    if (launch_gemm_tc<256, MPTP_GELU_EPI, MPTP_K13_NE>(m1, a1, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+    if (launch_gemm_tc<256, EPI_GELU, K13_NE>(m1, a1, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
-    // K2: row-parallel GEMM Z = sum_i Y_i B_i; K blocks of shard i are [i*f/t, (i+1)*f/t) / BK,
-    // visited for i = 0..t-1 in order, all into the same accumulator (the g sum).
-    const int fs = f / t;
+    // K2: row-parallel GEMM Z = sum_i Y_i B_i over the range; K blocks of shard i are
+    // [i*f/t, (i+1)*f/t) / BK, visited for i = s0..s0+n-1 in order, all into the same
+    // accumulator (the g sum).
     TmapSet m2{};
     int b2 = 0;
     if (!make_tmap_bf16(&m2.a, Y, f, T, f, 64, BM) || !(b2 = make_tmap_mn_operand(&m2.b, B, h, f, h)) ||
         !make_tmap_bf16_out(&m2.o0, Z, h, T, h))
         return MP_ERR_CUDA;
     GemmArgs a2 = launch_args(d_status);
-    a2.pr = problem(T, h, 256, 0 * (fs / BK), t * (fs / BK), false, true, Tb * f, hb * f);
+    a2.pr = problem(T, h, 256, c0 / BK, (c0 + nc) / BK, false, true, Tb * nc, hb * nc);
     a2.pr.b_mn = b2;
-    a2.out0 = reinterpret_cast<__nv_bfloat16*>(Z);
-    a2.ld_out0 = h;
-    if (launch_gemm_tc<256, MPTP_STORE_EPI, 4>(m2, a2, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+    if (launch_gemm_tc<256, EPI_STORE, 4>(m2, a2, sms, s) != cudaSuccess) return MP_ERR_CUDA;
     return MP_OK;
 }
 
-extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B, const mp_bf16* U,
-                                const mp_bf16* Y, const mp_bf16* dZ, mp_bf16* dX, mp_bf16* dA, mp_bf16* dB,
-                                mp_bf16* dU_ws, int T, int h, int f, int t, uint32_t* d_status, void* stream) {
+extern "C" mp_status mp_mlp_fwd(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B, mp_bf16* Z, mp_bf16* Y,
+                                mp_bf16* U_save, int T, int h, int f, int t, uint32_t* d_status, void* stream) {
+    return mp_mlp_fwd_shards(X, A, B, Z, Y, U_save, T, h, f, t, 0, t, d_status, stream);
+}
+
+extern "C" mp_status mp_mlp_bwd_shards(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B, const mp_bf16* U,
+                                       const mp_bf16* Y, const mp_bf16* dZ, mp_bf16* dX, mp_bf16* dA, mp_bf16* dB,
+                                       mp_bf16* dU_ws, int T, int h, int f, int t, int shard_begin, int shard_count,
+                                       uint32_t* d_status, void* stream) {
     mp_status st = check_mlp_shape(T, h, f, t);
     if (st != MP_OK) return st;
+    if ((st = check_shard_range(t, shard_begin, shard_count)) != MP_OK) return st;
     if (!A || !B || !dA || !dB) return MP_ERR_INVALID_ARG;
     if (T > 0 && (!X || !U || !Y || !dZ || !dX || !dU_ws)) return MP_ERR_INVALID_ARG;
     const void* ptrs[] = {X, A, B, U, Y, dZ, dX, dA, dB, dU_ws};
@@ -162,69 +163,64 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
     int sms = 0;
     if ((st = check_device(&sms)) != MP_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The range's columns of U, Y, dU, dA and rows of B, dB: [c0, c0 + nc).
+    const int fs = f / t;
+    const int c0 = shard_begin * fs, nc = shard_count * fs;
     if (T == 0) {
-        // Empty batch: the weight gradients are sums over zero tokens.
-        if (cudaMemsetAsync(dA, 0, size_t(h) * f * 2, s) != cudaSuccess ||
-            cudaMemsetAsync(dB, 0, size_t(f) * h * 2, s) != cudaSuccess)
+        // Empty batch: the range's weight gradients are sums over zero tokens.
+        if (cudaMemset2DAsync(dA + c0, size_t(f) * 2, 0, size_t(nc) * 2, size_t(h), s) != cudaSuccess ||
+            cudaMemsetAsync(dB + size_t(c0) * h, 0, size_t(nc) * h * 2, s) != cudaSuccess)
             return MP_ERR_CUDA;
         return MP_OK;
     }
-    const double Tb = 2.0 * T, hb = 2.0 * h, fb = 2.0 * f;
+    const double Tb = 2.0 * T, hb = 2.0 * h, fb = 2.0 * nc;
 
-    // K3: dU = (dZ B^T) * GeLU'(U).  A operand dZ [T,h] (K-major), B operand B [f,h] (K-major).
+    // K3: dU_r = (dZ B_r^T) * GeLU'(U_r).  A operand dZ [T,h] (K-major), B operand the range's rows
+    // of B [f,h] (K-major).
     TmapSet m3{};
-    if (!make_tmap_bf16(&m3.a, dZ, h, T, h, 64, BM) || !make_tmap_bf16(&m3.b, B, h, f, h, 64, 128) ||
-        !make_tmap_bf16_out(&m3.o0, dU_ws, f, T, f))
+    if (!make_tmap_bf16(&m3.a, dZ, h, T, h, 64, BM) || !make_tmap_bf16(&m3.b, B + size_t(c0) * h, h, nc, h, 64, 128) ||
+        !make_tmap_bf16_out(&m3.o0, dU_ws + c0, nc, T, f))
         return MP_ERR_CUDA;
     GemmArgs a3 = launch_args(d_status);
-    a3.pr = problem(T, f, 256, 0, h / BK, false, false, Tb * h, fb * h);
-    a3.aux = reinterpret_cast<const __nv_bfloat16*>(U);
+    a3.pr = problem(T, nc, 256, 0, h / BK, false, false, Tb * h, fb * h);
+    a3.aux = reinterpret_cast<const __nv_bfloat16*>(U + c0);
     a3.ld_aux = f;
-    a3.out0 = reinterpret_cast<__nv_bfloat16*>(dU_ws);
-    a3.ld_out0 = f;
-    if (launch_gemm_tc<256, MPTP_DGELU_EPI, MPTP_K13_NE>(m3, a3, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+    if (launch_gemm_tc<256, EPI_DGELU, K13_NE>(m3, a3, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
     // K4: dX = sum_i dU_i A_i^T.  A operand dU [T,f] (K-major), B operand A [h,f] (K-major); K blocks of
-    // shard i are [i*f/t, (i+1)*f/t) / BK, visited for i = 0..t-1 in order (the f sum).
-    const int fs = f / t;
+    // shard i are [i*f/t, (i+1)*f/t) / BK, visited for i = s0..s0+n-1 in order (the f sum).
     TmapSet m4{};
-    if (!make_tmap_bf16(&m4.a, dU_ws, f, T, f, 64, BM) || !make_tmap_bf16(&m4.b, A, f, h, f, 64, MPTP_K4_BN / 2) ||
+    if (!make_tmap_bf16(&m4.a, dU_ws, f, T, f, 64, BM) || !make_tmap_bf16(&m4.b, A, f, h, f, 64, K4_BN / 2) ||
         !make_tmap_bf16_out(&m4.o0, dX, h, T, h))
         return MP_ERR_CUDA;
     GemmArgs a4 = launch_args(d_status);
-    a4.pr = problem(T, h, MPTP_K4_BN, 0 * (fs / BK), t * (fs / BK), false, false, Tb * f, hb * f);
-    a4.out0 = reinterpret_cast<__nv_bfloat16*>(dX);
-    a4.ld_out0 = h;
+    a4.pr = problem(T, h, K4_BN, c0 / BK, (c0 + nc) / BK, false, false, Tb * nc, hb * nc);
 
-    // K5a: dA = X^T dU (M = h, N = f, K = T).  Both operands MN-major.
+    // K5a: dA_r = X^T dU_r (M = h, N = nc, K = T).  Both operands MN-major.
     TmapSet m5{};
     int a5f = 0, b5f = 0;
-    if (!(a5f = make_tmap_mn_operand(&m5.a, X, h, T, h)) || !(b5f = make_tmap_mn_operand(&m5.b, dU_ws, f, T, f)) ||
-        !make_tmap_bf16_out(&m5.o0, dA, f, h, f))
+    if (!(a5f = make_tmap_mn_operand(&m5.a, X, h, T, h)) ||
+        !(b5f = make_tmap_mn_operand(&m5.b, dU_ws + c0, nc, T, f)) || !make_tmap_bf16_out(&m5.o0, dA + c0, nc, h, f))
         return MP_ERR_CUDA;
     GemmArgs a5 = launch_args(d_status);
-    a5.pr = problem(h, f, 256, 0, ceil_div(T, BK), true, true, Tb * h, Tb * f);
+    a5.pr = problem(h, nc, 256, 0, ceil_div(T, BK), true, true, Tb * h, Tb * nc);
     a5.pr.a_mn = a5f;
     a5.pr.b_mn = b5f;
-    a5.out0 = reinterpret_cast<__nv_bfloat16*>(dA);
-    a5.ld_out0 = f;
 
-    // K5b: dB = Y^T dZ (M = f, N = h, K = T).  Both operands MN-major.
+    // K5b: dB_r = Y_r^T dZ (M = nc, N = h, K = T).  Both operands MN-major.
     TmapSet m6{};
     int a6f = 0, b6f = 0;
-    if (!(a6f = make_tmap_mn_operand(&m6.a, Y, f, T, f)) || !(b6f = make_tmap_mn_operand(&m6.b, dZ, h, T, h)) ||
-        !make_tmap_bf16_out(&m6.o0, dB, h, f, h))
+    if (!(a6f = make_tmap_mn_operand(&m6.a, Y + c0, nc, T, f)) || !(b6f = make_tmap_mn_operand(&m6.b, dZ, h, T, h)) ||
+        !make_tmap_bf16_out(&m6.o0, dB + size_t(c0) * h, h, nc, h))
         return MP_ERR_CUDA;
     GemmArgs a6 = launch_args(d_status);
-    a6.pr = problem(f, h, 256, 0, ceil_div(T, BK), true, true, Tb * f, Tb * h);
+    a6.pr = problem(nc, h, 256, 0, ceil_div(T, BK), true, true, Tb * nc, Tb * h);
     a6.pr.a_mn = a6f;
     a6.pr.b_mn = b6f;
-    a6.out0 = reinterpret_cast<__nv_bfloat16*>(dB);
-    a6.ld_out0 = h;
 
     // Every output tile is computed by the same K-loop whichever pairs run it, so both
     // schedules give bitwise identical results.
-    const int pairs = resident_pairs<256, MPTP_STORE_EPI, 4>(sms);
+    const int pairs = resident_pairs<256, EPI_STORE, 4>(sms);
     const int units[3] = {a4.pr.num_units, a5.pr.num_units, a6.pr.num_units};
     const int cost[3] = {a4.pr.kb_end - a4.pr.kb_begin + EPI_KB, a5.pr.kb_end - a5.pr.kb_begin + EPI_KB,
                          a6.pr.kb_end - a6.pr.kb_begin + EPI_KB};
@@ -243,9 +239,9 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
                       cudaStreamWaitEvent(ss->s[0], ss->fork, 0) == cudaSuccess &&
                       cudaStreamWaitEvent(ss->s[1], ss->fork, 0) == cudaSuccess;
             if (!ok) return MP_ERR_CUDA;
-            ok = launch_gemm_tc<MPTP_K4_BN, MPTP_STORE_EPI, 4>(m4, a4, sms, s, split[0]) == cudaSuccess;
-            ok = launch_gemm_tc<256, MPTP_STORE_EPI, 4>(m5, a5, sms, ss->s[0], split[1]) == cudaSuccess && ok;
-            ok = launch_gemm_tc<256, MPTP_STORE_EPI, 4>(m6, a6, sms, ss->s[1], split[2]) == cudaSuccess && ok;
+            ok = launch_gemm_tc<K4_BN, EPI_STORE, 4>(m4, a4, sms, s, split[0]) == cudaSuccess;
+            ok = launch_gemm_tc<256, EPI_STORE, 4>(m5, a5, sms, ss->s[0], split[1]) == cudaSuccess && ok;
+            ok = launch_gemm_tc<256, EPI_STORE, 4>(m6, a6, sms, ss->s[1], split[2]) == cudaSuccess && ok;
             // Join even after a failed launch, so the caller's stream never runs ahead of the side streams.
             for (int i = 0; i < 2; ++i)
                 ok = cudaEventRecord(ss->join[i], ss->s[i]) == cudaSuccess &&
@@ -253,9 +249,15 @@ extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf1
             return ok ? MP_OK : MP_ERR_CUDA;
         }
     }
-    if (launch_gemm_tc<MPTP_K4_BN, MPTP_STORE_EPI, 4>(m4, a4, sms, s) != cudaSuccess ||
-        launch_gemm_tc<256, MPTP_STORE_EPI, 4>(m5, a5, sms, s) != cudaSuccess ||
-        launch_gemm_tc<256, MPTP_STORE_EPI, 4>(m6, a6, sms, s) != cudaSuccess)
+    if (launch_gemm_tc<K4_BN, EPI_STORE, 4>(m4, a4, sms, s) != cudaSuccess ||
+        launch_gemm_tc<256, EPI_STORE, 4>(m5, a5, sms, s) != cudaSuccess ||
+        launch_gemm_tc<256, EPI_STORE, 4>(m6, a6, sms, s) != cudaSuccess)
         return MP_ERR_CUDA;
     return MP_OK;
+}
+
+extern "C" mp_status mp_mlp_bwd(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B, const mp_bf16* U,
+                                const mp_bf16* Y, const mp_bf16* dZ, mp_bf16* dX, mp_bf16* dA, mp_bf16* dB,
+                                mp_bf16* dU_ws, int T, int h, int f, int t, uint32_t* d_status, void* stream) {
+    return mp_mlp_bwd_shards(X, A, B, U, Y, dZ, dX, dA, dB, dU_ws, T, h, f, t, 0, t, d_status, stream);
 }
