@@ -24,9 +24,8 @@
 //               columns (TMEM lane quarter = warp % 4, thread = output row; with 8
 //               warps two warps share a quarter and split the columns), fused math,
 //               then bf16 rows staged in a 64-byte-swizzled shared box per warp and
-//               written by TMA stores (32x32 boxes), or stored straight from
-//               registers (the EPI_*_G forms, which leave room for one more
-//               pipeline stage), or cross-entropy partials. An accumulator is
+//               written by TMA stores (32x32 boxes), or cross-entropy partials.
+//               An accumulator is
 //               handed back (to the leader) as soon as its last columns are in
 //               registers, so it overlaps the next tile's MMAs.
 //
@@ -68,28 +67,19 @@ constexpr unsigned long long DRAIN_BUDGET_NS = 1000000000ull;  // 1 s
 constexpr unsigned long long ABORT_SETTLE_NS = 50000ull;       // in-flight copies land well within this
 
 enum EpiKind : int {
-    EPI_STORE = 0,  // out0 = bf16(acc)
-    EPI_GELU = 1,   // out0 = bf16(GeLU(acc)); out1 (nullable) = bf16(acc)
-    EPI_DGELU = 2,  // out0 = bf16(acc * GeLU'(aux)), aux = bf16 U
+    EPI_STORE = 0,  // o0 = bf16(acc)
+    EPI_GELU = 1,   // o0 = bf16(GeLU(acc)); o1 (when has_out1) = bf16(acc)
+    EPI_DGELU = 2,  // o0 = bf16(acc * GeLU'(aux)), aux = bf16 U
     EPI_CE = 3,     // per-row online max / sum-exp / target logit over the unit
-    EPI_DZ = 4,     // out0 = bf16(dloss * (exp(acc - lse) - [col == target])), 0 on padding columns
-    EPI_ACC = 5,    // fp32 accumulation across launches into `acc`; the last launch stores bf16 out0
-    EPI_STORE_G = 6,  // as EPI_STORE, GELU, DGELU, but rows stored from registers: no staging
-    EPI_GELU_G = 7,   // boxes, so the shared memory they took holds one more pipeline stage
-    EPI_DGELU_G = 8,
+    EPI_DZ = 4,     // o0 = bf16(dloss * (exp(acc - lse) - [col == target])), 0 on padding columns
+    EPI_ACC = 5,    // fp32 accumulation across launches into `acc`; the last launch stores bf16 o0
 };
-
-// Register-store (direct) form of an epilogue, and the math it shares with the staged form.
-__host__ __device__ constexpr bool epi_direct(int e) { return e == EPI_STORE_G || e == EPI_GELU_G || e == EPI_DGELU_G; }
-__host__ __device__ constexpr int epi_math(int e) {
-    return e == EPI_STORE_G ? EPI_STORE : e == EPI_GELU_G ? EPI_GELU : e == EPI_DGELU_G ? EPI_DGELU : e;
-}
 
 enum AccMode : int {
     ACC_FIRST = 0,  // acc = C
     ACC_MID = 1,    // acc += C
-    ACC_LAST = 2,   // out0 = bf16(acc + C)
-    ACC_ONLY = 3,   // out0 = bf16(C)
+    ACC_LAST = 2,   // o0 = bf16(acc + C)
+    ACC_ONLY = 3,   // o0 = bf16(C)
 };
 
 // The GEMM of a launch.
@@ -121,11 +111,6 @@ struct GemmArgs {
     float* acc;
     long long ld_acc;
     int acc_mode;
-    // register-store epilogues: out0 (and for GeLU out1 = U) with their row pitches
-    __nv_bfloat16* out0;
-    long long ld_out0;
-    __nv_bfloat16* out1;
-    long long ld_out1;
     uint32_t* status;         // nullable
     unsigned long long budget_ns;
 };
@@ -150,7 +135,7 @@ struct GemmCfg {
     static constexpr int B_BYTES = BNH * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TMEM_COLS = BN <= 128 ? 256 : 512;  // two accumulators, power of two
-    static constexpr int STG_BYTES = (EPI == EPI_CE || epi_direct(EPI)) ? 0 : NE * STG_BYTES_PER_WARP;
+    static constexpr int STG_BYTES = EPI == EPI_CE ? 0 : NE * STG_BYTES_PER_WARP;
     static constexpr int MAX_STAGES = 8;
     static constexpr int FIT_STAGES = static_cast<int>((SMEM_LIMIT - 1024 - 512 - STG_BYTES) / STAGE_BYTES);
     static constexpr int STAGES = FIT_STAGES < MAX_STAGES ? FIT_STAGES : MAX_STAGES;
@@ -347,7 +332,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&maps.a);
         prefetch_tensormap(&maps.b);
-        if (EPI != EPI_CE && !epi_direct(EPI)) prefetch_tensormap(&maps.o0);
+        if (EPI != EPI_CE) prefetch_tensormap(&maps.o0);
         if (EPI == EPI_GELU && args.has_out1) prefetch_tensormap(&maps.o1);
     }
     if (warp == 1) {
@@ -531,7 +516,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                 // chunk cc+1 is in flight while chunk cc is computed and stored.
                 auto issue = [&](int cc, uint32_t (&rr)[32], uint32_t (&uu)[16]) {
                     const int c = c_begin + cc;
-                    if constexpr (epi_math(EPI) == EPI_DGELU) {
+                    if constexpr (EPI == EPI_DGELU) {
                         const int col0 = n_blk * BN + c * 32;
                         if (row_ok && col0 < p.N) {
                             const uint4* src = reinterpret_cast<const uint4*>(args.aux + row * args.ld_aux + col0);
@@ -554,41 +539,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                     const int c = c_begin + cc;
                     const int col0 = n_blk * BN + c * 32;
                     if (col0 >= p.N) return;  // ragged N tail (whole 32-column chunks)
-                    // One 32-column bf16 row segment: staged and TMA-stored, or (register-store
-                    // forms) 64 contiguous bytes written as four 16-byte stores.
-                    auto emit = [&](const CUtensorMap* map, __nv_bfloat16* out, long long ld, const uint32_t (&pk)[16]) {
-                        if constexpr (epi_direct(EPI)) {
-                            if (row_ok) {
-                                uint4* dst = reinterpret_cast<uint4*>(out + static_cast<long long>(row) * ld + col0);
-#pragma unroll
-                                for (int j = 0; j < 4; ++j)
-                                    dst[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-                            }
-                        } else {
-                            stage_and_store(map, stg, sbuf, lane, pk, col0, row0);
-                        }
-                    };
-                    if constexpr (epi_math(EPI) == EPI_STORE) {
+                    // One 32-column bf16 row segment per thread, staged and TMA-stored.
+                    if constexpr (EPI == EPI_STORE) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                        emit(tmO0, args.out0, args.ld_out0, pk);
-                    } else if constexpr (epi_math(EPI) == EPI_GELU) {
+                        stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
+                    } else if constexpr (EPI == EPI_GELU) {
                         uint32_t pk[16];
                         if (args.has_out1) {
 #pragma unroll
                             for (int j = 0; j < 16; ++j)
                                 pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-                            emit(&maps.o1, args.out1, args.ld_out1, pk);
+                            stage_and_store(&maps.o1, stg, sbuf, lane, pk, col0, row0);
                         }
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const float2 g = gelu2(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])));
                             pk[j] = pack_bf16x2(g.x, g.y);
                         }
-                        emit(tmO0, args.out0, args.ld_out0, pk);
-                    } else if constexpr (epi_math(EPI) == EPI_DGELU) {
+                        stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
+                    } else if constexpr (EPI == EPI_DGELU) {
                         uint32_t pk[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
@@ -596,7 +568,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
                             const float2 g = mul2(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), gp);
                             pk[j] = pack_bf16x2(g.x, g.y);
                         }
-                        emit(tmO0, args.out0, args.ld_out0, pk);
+                        stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
                     } else if constexpr (EPI == EPI_DZ) {
                         // dZ = dloss * (softmax - onehot) on valid columns, 0 on padding.
                         constexpr float LOG2E = 1.4426950408889634f;
@@ -721,7 +693,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
             }
         }
         // All of this warp's TMA stores must have landed before the kernel ends.
-        if (EPI != EPI_CE && !epi_direct(EPI) && lane == 0) bulk_wait_group<0>();
+        if (EPI != EPI_CE && lane == 0) bulk_wait_group<0>();
     }
 
     // ---------------- teardown ----------------
@@ -765,12 +737,6 @@ inline int resident_pairs(int num_sms) {
     return clusters;
 }
 
-// MPTP_BALANCE_PAIRS=0 launches every resident pair even when fewer give the same rounds.
-inline bool balance_pairs() {
-    const char* v = std::getenv("MPTP_BALANCE_PAIRS");
-    return !(v != nullptr && v[0] == '0');
-}
-
 // Host-side launcher: grid = 2 x min(units, resident pairs, max_pairs if > 0), one CTA per SM.
 template <int BN, int EPI, int NE>
 inline cudaError_t launch_gemm_tc(const TmapSet& maps, const GemmArgs& args, int num_sms, cudaStream_t stream,
@@ -787,7 +753,7 @@ inline cudaError_t launch_gemm_tc(const TmapSet& maps, const GemmArgs& args, int
     int use = args.pr.num_units < pairs ? args.pr.num_units : pairs;
     // As few pairs as give the same number of rounds of units: the same time, and the idle
     // SMs leave power headroom to the busy ones under the board's power cap.
-    if (use > 0 && balance_pairs()) {
+    if (use > 0) {
         const int rounds = (args.pr.num_units + use - 1) / use;
         use = (args.pr.num_units + rounds - 1) / rounds;
     }
