@@ -27,6 +27,7 @@
 #include <cstring>
 
 #include "mptp_gemm.cuh"
+#include "mptp_gemm_split.cuh"
 #include "mptp_internal.h"
 
 namespace mptp {
@@ -75,13 +76,53 @@ static BwdSchedule bwd_schedule() {
 // Cost of one output tile in K-block times: its K blocks plus about two for the epilogue.
 constexpr int EPI_KB = 2;
 
-// Epilogue warps of K1 and K3 (four measured 0.2-0.8 % faster than eight).
-constexpr int K13_NE = 4;
+// Epilogue warps of K1 and K3 (GeLU, GeLU'). A launch's last tile is epilogued after its last
+// MMA with nothing to hide behind: with few K blocks per CTA pair (the layer at T = 2048,
+// h = 1536: 72 a pair) eight warps halve that tail (K3's 10.6 -> 6.3 us, K1's 5.4 -> 4.0 us;
+// the step -1 %), while on long launches four measured 0.2-0.8 % faster (fewer warps beside the
+// MMA issuer). The store-only GEMMs keep four: eight were 1 % slower there.
+constexpr int SHORT_LAUNCH_KB = 256;  // K blocks a pair runs, at most, for eight epilogue warps
+
+template <int EPI>
+static cudaError_t launch_gelu_epi(const TmapSet& m, const GemmArgs& a, int sms, cudaStream_t s) {
+    const int pairs = resident_pairs<256, EPI, 4>(sms);
+    const bool short_launch = ceil_div(a.pr.num_units, pairs) * (a.pr.kb_end - a.pr.kb_begin) <= SHORT_LAUNCH_KB;
+    return short_launch ? launch_gemm_tc<256, EPI, 8>(m, a, sms, s) : launch_gemm_tc<256, EPI, 4>(m, a, sms, s);
+}
 
 // Tile width of K4 (dX = dU A^T, N = h, B operand K-major). 224-wide tiles cut h = 3072
 // into 14 column units instead of 12, so T = 4096 gives 224 units: 2.95 rounds of 76 CTA
 // pairs, against 2.53 rounds of 256-wide tiles whose last round leaves half the pairs idle.
 constexpr int K4_BN = 224;
+
+// Split-K for the row-parallel GEMMs (K2, K4) when their output tiles do not fill the chip:
+// the two CTA pairs of a cluster share a 256-wide tile, each over half of the shard-ordered K
+// range, and the partials are summed on chip (mptp_gemm_split.cuh). Costs in K-block times:
+// one pair per tile, `bn` wide, takes rounds x L x bn / 256; two pairs take
+// rounds x ceil(L / 2) plus about SPLIT_HOP_KB for the on-chip sum. The split is taken when it
+// is at least 10 % cheaper and each pair keeps at least 16 K blocks (T = 2048, h = 3072: 96
+// tiles on 36 clusters, 292 against 384; the forward 5.6 % faster). Measured and not kept:
+// 128-wide split tiles (at T = 2048, h = 1536 the forward took 81 us against 68 us unsplit), and
+// clusters of three or four pairs, which fit only 23 or 15 at a time on the 152-SM GB300 and beat
+// two pairs at no layer shape of the Megatron-LM sweep.
+constexpr int SPLIT_PAIRS = 2;
+constexpr int SPLIT_HOP_KB = 4;
+constexpr int SPLIT_MIN_KB = 16;
+
+static long long tiles_of(int M, int N, int bn) { return static_cast<long long>(ceil_div(M, 2 * BM)) * ceil_div(N, bn); }
+
+// True when the split kernel should run this GEMM (M x N, L K blocks) instead of the
+// single-pair kernel with BN1-wide tiles.
+template <int BN1>
+static bool use_split(int M, int N, int L, int sms) {
+    const int pairs = resident_pairs<BN1, EPI_STORE, 4>(sms);
+    const int clusters = resident_split_clusters<256, SPLIT_PAIRS>(sms);
+    if (clusters <= 0 || L < SPLIT_MIN_KB * SPLIT_PAIRS) return false;
+    const long long one = (tiles_of(M, N, BN1) + pairs - 1) / pairs * L * BN1;  // x 1/256 K-block times
+    const long long two =
+        ((tiles_of(M, N, 256) + clusters - 1) / clusters * ceil_div(L, SPLIT_PAIRS) + SPLIT_HOP_KB) * 256;
+    return two * 10 <= one * 9;
+}
 
 static GemmArgs launch_args(uint32_t* status) {
     GemmArgs a{};
@@ -125,7 +166,7 @@ extern "C" mp_status mp_mlp_fwd_shards(const mp_bf16* X, const mp_bf16* A, const
     a1.pr = problem(T, nc, 256, 0, h / BK, false, true, Tb * h, hb * nc);
     a1.pr.b_mn = b1;
     a1.has_out1 = U_save ? 1 : 0;
-    if (launch_gemm_tc<256, EPI_GELU, K13_NE>(m1, a1, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+    if (launch_gelu_epi<EPI_GELU>(m1, a1, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
     // K2: row-parallel GEMM Z = sum_i Y_i B_i over the range; K blocks of shard i are
     // [i*f/t, (i+1)*f/t) / BK, visited for i = s0..s0+n-1 in order, all into the same
@@ -138,7 +179,10 @@ extern "C" mp_status mp_mlp_fwd_shards(const mp_bf16* X, const mp_bf16* A, const
     GemmArgs a2 = launch_args(d_status);
     a2.pr = problem(T, h, 256, c0 / BK, (c0 + nc) / BK, false, true, Tb * nc, hb * nc);
     a2.pr.b_mn = b2;
-    if (launch_gemm_tc<256, EPI_STORE, 4>(m2, a2, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+    const bool split2 = use_split<256>(T, h, nc / BK, sms);
+    if ((split2 ? launch_gemm_split<256, SPLIT_PAIRS>(m2, a2, sms, s) : launch_gemm_tc<256, EPI_STORE, 4>(m2, a2, sms, s)) !=
+        cudaSuccess)
+        return MP_ERR_CUDA;
     return MP_OK;
 }
 
@@ -185,7 +229,7 @@ extern "C" mp_status mp_mlp_bwd_shards(const mp_bf16* X, const mp_bf16* A, const
     a3.pr = problem(T, nc, 256, 0, h / BK, false, false, Tb * h, fb * h);
     a3.aux = reinterpret_cast<const __nv_bfloat16*>(U + c0);
     a3.ld_aux = f;
-    if (launch_gemm_tc<256, EPI_DGELU, K13_NE>(m3, a3, sms, s) != cudaSuccess) return MP_ERR_CUDA;
+    if (launch_gelu_epi<EPI_DGELU>(m3, a3, sms, s) != cudaSuccess) return MP_ERR_CUDA;
 
     // K4: dX = sum_i dU_i A_i^T.  A operand dU [T,f] (K-major), B operand A [h,f] (K-major); K blocks of
     // shard i are [i*f/t, (i+1)*f/t) / BK, visited for i = s0..s0+n-1 in order (the f sum).
@@ -249,7 +293,14 @@ extern "C" mp_status mp_mlp_bwd_shards(const mp_bf16* X, const mp_bf16* A, const
             return ok ? MP_OK : MP_ERR_CUDA;
         }
     }
-    if (launch_gemm_tc<K4_BN, EPI_STORE, 4>(m4, a4, sms, s) != cudaSuccess ||
+    const bool split4 = use_split<K4_BN>(T, h, nc / BK, sms);
+    if (split4) {
+        // The split kernel's 256-wide tiles: B boxes of 128 rows per CTA.
+        if (!make_tmap_bf16(&m4.b, A, f, h, f, 64, 128)) return MP_ERR_CUDA;
+        a4.pr = problem(T, h, 256, c0 / BK, (c0 + nc) / BK, false, false, Tb * nc, hb * nc);
+    }
+    if ((split4 ? launch_gemm_split<256, SPLIT_PAIRS>(m4, a4, sms, s) : launch_gemm_tc<K4_BN, EPI_STORE, 4>(m4, a4, sms, s)) !=
+            cudaSuccess ||
         launch_gemm_tc<256, EPI_STORE, 4>(m5, a5, sms, s) != cudaSuccess ||
         launch_gemm_tc<256, EPI_STORE, 4>(m6, a6, sms, s) != cudaSuccess)
         return MP_ERR_CUDA;
