@@ -506,15 +506,22 @@ def time_next_rows(step, reps, flush):
     dloss = torch.full((T,), 1.0 / T, dtype=torch.float32, device=d["Xc"].device)
     dXc = torch.empty(T, h, dtype=torch.bfloat16, device=d["Xc"].device)
     dE = torch.empty(v_pad, h, dtype=torch.bfloat16, device=d["Xc"].device)
-    mp.mp_vocab_ce(d["Xc"], d["E"], d["target"], d["loss"], step.ws, v_valid=v_valid, t=t)
-    # Both workspace sizes: the minimum (one shard of dZ at a time) and the one-pass size
-    # (every shard's dZ: one GEMM of each kind).
+    lse = torch.empty(T, dtype=torch.float32, device=d["Xc"].device)
+    mp.mp_vocab_ce_lse(d["Xc"], d["E"], d["target"], d["loss"], lse, step.ws, v_valid=v_valid, t=t)
+    # From the forward's exported log-sum-exp, in both workspace sizes: the minimum (one shard of
+    # dZ at a time) and the one-pass size (every shard's dZ: one GEMM of each kind); and from the
+    # forward's loss (the log-sum-exp rebuilt first), one pass.
     ce_ms = {}
-    for mode, size in (("shard_by_shard", mp.mp_vocab_ce_bwd_workspace_bytes),
-                       ("one_pass", mp.mp_vocab_ce_bwd_workspace_bytes_one_pass)):
+    for mode, size, from_lse in (("shard_by_shard", mp.mp_vocab_ce_bwd_workspace_bytes, True),
+                                 ("one_pass", mp.mp_vocab_ce_bwd_workspace_bytes_one_pass, True),
+                                 ("one_pass_from_loss", mp.mp_vocab_ce_bwd_workspace_bytes_one_pass, False)):
         wsb = torch.empty(size(T, h, v_pad, t), dtype=torch.uint8, device=d["Xc"].device)
-        fn = lambda: mp.mp_vocab_ce_bwd(d["Xc"], d["E"], d["target"], d["loss"], dloss, dXc, dE, wsb,
-                                        v_valid=v_valid, t=t, d_status=step.status)
+        if from_lse:
+            fn = lambda: mp.mp_vocab_ce_bwd_lse(d["Xc"], d["E"], d["target"], lse, dloss, dXc, dE, wsb,
+                                                v_valid=v_valid, t=t, d_status=step.status)
+        else:
+            fn = lambda: mp.mp_vocab_ce_bwd(d["Xc"], d["E"], d["target"], d["loss"], dloss, dXc, dE, wsb,
+                                            v_valid=v_valid, t=t, d_status=step.status)
         fn()
         ce_ms[mode] = event_median(fn, reps, flush)
         step.check_status()
@@ -560,8 +567,9 @@ def time_next_rows(step, reps, flush):
     executed = 6.0 * T * h * v_pad  # plus the logit recompute (logits are never stored)
     return {"ce_bwd": {"ms": ms, "tflops_algorithmic": algo / (ms * 1e-3) / 1e12,
                        "tflops_executed": executed / (ms * 1e-3) / 1e12, "tokens_per_s": T / (ms * 1e-3),
-                       "ms_shard_by_shard": ce_ms["shard_by_shard"],
-                       "flop_note": "one-pass workspace; algorithmic 4Thv (dX, dE), executed adds the 2Thv recompute"},
+                       "ms_shard_by_shard": ce_ms["shard_by_shard"], "ms_from_loss": ce_ms["one_pass_from_loss"],
+                       "flop_note": "from the exported lse, one-pass workspace; algorithmic 4Thv (dX, dE), "
+                                    "executed adds the 2Thv logit recompute"},
             "vocab_embed": embed,
             "attn_fwd": attn}
 

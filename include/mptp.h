@@ -204,6 +204,15 @@ MP_API mp_status mp_vocab_ce_combine(const void* workspace, size_t workspace_byt
                               int T, int v_pad, int v_valid, int t,
                               uint32_t* d_status, void* stream);
 
+/* mp_vocab_ce that also writes the per-token log-sum-exp over the valid vocabulary,
+ * lse[r] = M + log S (fp32 [T], device memory, required when T > 0), the quantity the
+ * backward needs (mp_vocab_ce_bwd_lse). lse is NaN for a token whose target is outside
+ * [0, v_valid) (that token contributes no gradient). loss is bit for bit mp_vocab_ce's. */
+MP_API mp_status mp_vocab_ce_lse(const mp_bf16* X, const mp_bf16* E, const int32_t* target,
+                          float* loss, float* lse, void* workspace, size_t workspace_bytes,
+                          int T, int h, int v_pad, int v_valid, int t,
+                          uint32_t* d_status, void* stream);
+
 /*
  * Backward of the vocab-parallel cross-entropy. The pages describe the fused
  * forward only; this is the plain derivative of softmax cross-entropy, computed
@@ -236,6 +245,16 @@ MP_API mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const int32
                           mp_bf16* dX, mp_bf16* dE, void* workspace, size_t workspace_bytes,
                           int T, int h, int v_pad, int v_valid, int t,
                           uint32_t* d_status, void* stream);
+
+/* mp_vocab_ce_bwd from the forward's exported log-sum-exp (mp_vocab_ce_lse) instead of its
+ * loss: no recompute of the target logits (one launch fewer). Same workspace sizes, outputs
+ * and rules; a NaN lse marks a token with an invalid target, which gets no gradient (the
+ * forward set MP_DEV_TARGET_RANGE for it). */
+MP_API mp_status mp_vocab_ce_bwd_lse(const mp_bf16* X, const mp_bf16* E, const int32_t* target,
+                              const float* lse, const float* dloss,
+                              mp_bf16* dX, mp_bf16* dE, void* workspace, size_t workspace_bytes,
+                              int T, int h, int v_pad, int v_valid, int t,
+                              uint32_t* d_status, void* stream);
 
 /*
  * Vocab-parallel input embedding ("Megatron-LM: Training Multi-Billion Parameter

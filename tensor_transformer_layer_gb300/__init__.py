@@ -34,7 +34,7 @@ STATUS_NAMES = {
 EXPORTS = ("mp_mlp_fwd", "mp_mlp_bwd", "mp_mlp_fwd_shards", "mp_mlp_bwd_shards", "mp_vocab_ce_workspace_bytes", "mp_vocab_ce", "mp_vocab_ce_partials",
            "mp_vocab_ce_combine", "mp_status_string", "mp_status_from_device", "mp_version",
            "mp_vocab_ce_noalloc", "mp_vocab_ce_bwd_workspace_bytes", "mp_vocab_ce_bwd_workspace_bytes_one_pass",
-           "mp_vocab_ce_bwd", "mp_vocab_embed",
+           "mp_vocab_ce_bwd", "mp_vocab_ce_lse", "mp_vocab_ce_bwd_lse", "mp_vocab_embed",
            "mp_attn_fwd")
 
 
@@ -79,6 +79,10 @@ def lib() -> ctypes.CDLL:
         L.mp_vocab_ce_bwd_workspace_bytes_one_pass.restype = ctypes.c_size_t
         L.mp_vocab_ce_bwd.argtypes = [_P] * 7 + [_P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P, _P]
         L.mp_vocab_ce_bwd.restype = _I
+        L.mp_vocab_ce_lse.argtypes = [_P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P, _P]
+        L.mp_vocab_ce_lse.restype = _I
+        L.mp_vocab_ce_bwd_lse.argtypes = [_P] * 7 + [_P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P, _P]
+        L.mp_vocab_ce_bwd_lse.restype = _I
         L.mp_attn_fwd.argtypes = [_P] * 6 + [_I, _I, _I, _I, _I, _P, _P]
         L.mp_attn_fwd.restype = _I
         L.mp_vocab_embed.argtypes = [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P]
@@ -214,6 +218,19 @@ def mp_vocab_ce(X, E, target, loss, workspace, *, v_valid: int, t: int, d_status
     _check("mp_vocab_ce", code)
 
 
+def mp_vocab_ce_lse(X, E, target, loss, lse, workspace, *, v_valid: int, t: int, d_status=None, stream=None) -> None:
+    """mp_vocab_ce that also writes the per-token log-sum-exp lse[T] fp32 (NaN for invalid targets)."""
+    T, h = X.shape
+    v_pad = E.shape[0]
+    wp, wb = _ws(workspace)
+    code = lib().mp_vocab_ce_lse(
+        _ptr(X, "X", shape=(T, h)), _ptr(E, "E", shape=(v_pad, h)),
+        _ptr(target, "target", dtype=torch.int32, shape=(T,)), _ptr(loss, "loss", dtype=torch.float32, shape=(T,)),
+        _ptr(lse, "lse", dtype=torch.float32, shape=(T,)), wp, wb, T, h, v_pad, int(v_valid), int(t),
+        _status_ptr(d_status), _stream(stream))
+    _check("mp_vocab_ce_lse", code)
+
+
 def mp_vocab_ce_partials(X, E, target, workspace, *, v_valid: int, t: int, d_status=None, stream=None) -> None:
     T, h = X.shape
     v_pad = E.shape[0]
@@ -270,6 +287,21 @@ def mp_vocab_ce_bwd(X, E, target, loss, dloss, dX, dE, workspace, *, v_valid: in
         _ptr(dE, "dE", shape=(v_pad, h)), wp, wb, T, h, v_pad, int(v_valid), int(t), _status_ptr(d_status),
         _stream(stream))
     _check("mp_vocab_ce_bwd", code)
+
+
+def mp_vocab_ce_bwd_lse(X, E, target, lse, dloss, dX, dE, workspace, *, v_valid: int, t: int, d_status=None,
+                        stream=None) -> None:
+    """Backward of the fused cross-entropy from the forward's exported log-sum-exp."""
+    T, h = X.shape
+    v_pad = E.shape[0]
+    wp, wb = _ws(workspace)
+    code = lib().mp_vocab_ce_bwd_lse(
+        _ptr(X, "X", shape=(T, h)), _ptr(E, "E", shape=(v_pad, h)),
+        _ptr(target, "target", dtype=torch.int32, shape=(T,)), _ptr(lse, "lse", dtype=torch.float32, shape=(T,)),
+        _ptr(dloss, "dloss", dtype=torch.float32, shape=(T,)), _ptr(dX, "dX", shape=(T, h)),
+        _ptr(dE, "dE", shape=(v_pad, h)), wp, wb, T, h, v_pad, int(v_valid), int(t), _status_ptr(d_status),
+        _stream(stream))
+    _check("mp_vocab_ce_bwd_lse", code)
 
 
 def mp_vocab_embed(ids, E, out, *, v_valid: int, t: int, d_status=None, stream=None) -> None:

@@ -7,7 +7,8 @@
 //       epilogue keeps, per token, the running max m_p, the sum of exp(z - m_p)
 //       and the target logit, and writes the triple; logits stay on chip.
 //   K7  per token: M = max_p m_p, S = sum_p s_p exp(m_p - M),
-//       loss = M + log S - z_target (the page's two all-reduces and final step).
+//       loss = M + log S - z_target (the page's two all-reduces and final step); on request
+//       also lse = M + log S, the per-token log-sum-exp the backward needs.
 #include "mptp_gemm.cuh"
 #include "mptp_internal.h"
 
@@ -41,7 +42,8 @@ __device__ __forceinline__ void lse_fold(float& M, float& S, const float (&mm)[C
 template <bool SPLIT>
 __global__ void __launch_bounds__(32 * CMB_WARPS) ce_combine_kernel(const float* __restrict__ ws,
                                                                     const int32_t* __restrict__ target,
-                                                                    float* __restrict__ loss, int T, int P, int G,
+                                                                    float* __restrict__ loss,
+                                                                    float* __restrict__ lse_out, int T, int P, int G,
                                                                     int chunk_cols, int v_valid, uint32_t* status) {
     grid_dependency_wait();  // the partials of the logit GEMM before it
     __shared__ float sM[SPLIT ? CMB_WARPS : 1][32], sS[SPLIT ? CMB_WARPS : 1][32];
@@ -85,11 +87,14 @@ __global__ void __launch_bounds__(32 * CMB_WARPS) ce_combine_kernel(const float*
     const int tg = target[r];
     if (tg < 0 || tg >= v_valid) {
         loss[r] = __int_as_float(0x7fc00000);
+        if (lse_out) lse_out[r] = __int_as_float(0x7fc00000);  // no gradient flows from this token
         if (status) atomicOr(status, DEV_TARGET_RANGE);
         return;
     }
     const float z = ws[(tg / chunk_cols) * stride + 2ll * T + r];
-    loss[r] = M + logf(S) - z;
+    const float l = M + logf(S);
+    loss[r] = l - z;
+    if (lse_out) lse_out[r] = l;
 }
 static_assert(CMB_WARPS <= CMB_LOADS, "a group's merge folds up to CMB_WARPS pairs in one pass");
 
@@ -160,14 +165,13 @@ extern "C" mp_status mp_vocab_ce_partials(const mp_bf16* X, const mp_bf16* E, co
     return e == cudaSuccess ? MP_OK : MP_ERR_CUDA;
 }
 
-extern "C" mp_status mp_vocab_ce_combine(const void* workspace, size_t workspace_bytes, const int32_t* target,
-                                         float* loss, int T, int v_pad, int v_valid, int t, uint32_t* d_status,
-                                         void* stream) {
+static mp_status ce_combine(const void* workspace, size_t workspace_bytes, const int32_t* target, float* loss,
+                            float* lse, int T, int v_pad, int v_valid, int t, uint32_t* d_status, void* stream) {
     if (T < 0 || v_pad <= 0 || t < 1 || v_valid < 1) return MP_ERR_INVALID_ARG;
     if (v_pad % (128 * t) != 0 || v_valid > v_pad) return MP_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return MP_OK;
     if (!workspace || !target || !loss) return MP_ERR_INVALID_ARG;
-    if (!aligned16(workspace) || !aligned16(target) || !aligned16(loss) ||
+    if (!aligned16(workspace) || !aligned16(target) || !aligned16(loss) || (lse && !aligned16(lse)) ||
         (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)))
         return MP_ERR_MISALIGNED;
     if (workspace_bytes < mp_vocab_ce_workspace_bytes(T, v_pad, t)) return MP_ERR_WORKSPACE;
@@ -181,19 +185,39 @@ extern "C" mp_status mp_vocab_ce_combine(const void* workspace, size_t workspace
     const cudaError_t e = launch_pdl(G > 1 ? ce_combine_kernel<true> : ce_combine_kernel<false>,
                                      dim3(ceil_div(T, 32 * (W / G))), dim3(32 * W),
                                      0, static_cast<cudaStream_t>(stream), static_cast<const float*>(workspace),
-                                     target, loss, T, plan.P, G, plan.chunk_cols, v_valid, d_status);
+                                     target, loss, lse, T, plan.P, G, plan.chunk_cols, v_valid, d_status);
     return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? MP_OK : MP_ERR_CUDA;
+}
+
+extern "C" mp_status mp_vocab_ce_combine(const void* workspace, size_t workspace_bytes, const int32_t* target,
+                                         float* loss, int T, int v_pad, int v_valid, int t, uint32_t* d_status,
+                                         void* stream) {
+    return ce_combine(workspace, workspace_bytes, target, loss, nullptr, T, v_pad, v_valid, t, d_status, stream);
+}
+
+static mp_status vocab_ce(const mp_bf16* X, const mp_bf16* E, const int32_t* target, float* loss, float* lse,
+                          void* workspace, size_t workspace_bytes, int T, int h, int v_pad, int v_valid, int t,
+                          uint32_t* d_status, void* stream) {
+    mp_status st = check_ce_shape(T, h, v_pad, v_valid, t);
+    if (st != MP_OK) return st;
+    if (T == 0) return MP_OK;
+    if (!loss) return MP_ERR_INVALID_ARG;
+    if (!aligned16(loss) || (lse && !aligned16(lse))) return MP_ERR_MISALIGNED;
+    st = mp_vocab_ce_partials(X, E, target, workspace, workspace_bytes, T, h, v_pad, v_valid, t, d_status, stream);
+    if (st != MP_OK) return st;
+    return ce_combine(workspace, workspace_bytes, target, loss, lse, T, v_pad, v_valid, t, d_status, stream);
 }
 
 extern "C" mp_status mp_vocab_ce(const mp_bf16* X, const mp_bf16* E, const int32_t* target, float* loss,
                                  void* workspace, size_t workspace_bytes, int T, int h, int v_pad, int v_valid,
                                  int t, uint32_t* d_status, void* stream) {
-    mp_status st = check_ce_shape(T, h, v_pad, v_valid, t);
-    if (st != MP_OK) return st;
-    if (T == 0) return MP_OK;
-    if (!loss) return MP_ERR_INVALID_ARG;
-    if (!aligned16(loss)) return MP_ERR_MISALIGNED;
-    st = mp_vocab_ce_partials(X, E, target, workspace, workspace_bytes, T, h, v_pad, v_valid, t, d_status, stream);
-    if (st != MP_OK) return st;
-    return mp_vocab_ce_combine(workspace, workspace_bytes, target, loss, T, v_pad, v_valid, t, d_status, stream);
+    return vocab_ce(X, E, target, loss, nullptr, workspace, workspace_bytes, T, h, v_pad, v_valid, t, d_status,
+                    stream);
+}
+
+extern "C" mp_status mp_vocab_ce_lse(const mp_bf16* X, const mp_bf16* E, const int32_t* target, float* loss,
+                                     float* lse, void* workspace, size_t workspace_bytes, int T, int h, int v_pad,
+                                     int v_valid, int t, uint32_t* d_status, void* stream) {
+    if (T > 0 && !lse) return MP_ERR_INVALID_ARG;
+    return vocab_ce(X, E, target, loss, lse, workspace, workspace_bytes, T, h, v_pad, v_valid, t, d_status, stream);
 }

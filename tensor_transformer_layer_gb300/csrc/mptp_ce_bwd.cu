@@ -11,8 +11,9 @@
 //   K11  dE_i = dZ_i^T X  (both operands MN-major);
 //   K12  dX += dZ_i E_i   (fp32 accumulation across shards in shard order - the sum the
 //        forward's all-reduce would carry - and one bf16 store after the last shard).
-// The log-sum-exp comes from the forward's loss: lse = loss + z_target, with z_target
-// = X[r] . E[target[r]] recomputed in fp32 (K9).
+// The log-sum-exp comes from the forward: either exported by it (mp_vocab_ce_lse, then
+// mp_vocab_ce_bwd_lse), or rebuilt from its loss: lse = loss + z_target, with z_target
+// = X[r] . E[target[r]] recomputed in fp32 (K9, mp_vocab_ce_bwd).
 #include "mptp_gemm.cuh"
 #include "mptp_internal.h"
 
@@ -91,15 +92,16 @@ extern "C" size_t mp_vocab_ce_bwd_workspace_bytes_one_pass(int T, int h, int v_p
     return L.total;
 }
 
-extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const int32_t* target, const float* loss,
-                                     const float* dloss, mp_bf16* dX, mp_bf16* dE, void* workspace,
-                                     size_t workspace_bytes, int T, int h, int v_pad, int v_valid, int t,
-                                     uint32_t* d_status, void* stream) {
+// The backward from either the forward's loss (lse rebuilt by K9) or its exported lse.
+static mp_status ce_bwd(const mp_bf16* X, const mp_bf16* E, const int32_t* target, const float* loss,
+                        const float* lse_in, const float* dloss, mp_bf16* dX, mp_bf16* dE, void* workspace,
+                        size_t workspace_bytes, int T, int h, int v_pad, int v_valid, int t, uint32_t* d_status,
+                        void* stream) {
     if (T < 0 || h <= 0 || v_pad <= 0 || t < 1 || v_valid < 1) return MP_ERR_INVALID_ARG;
     if (h % 64 != 0 || v_pad % (128 * t) != 0 || v_valid > v_pad) return MP_ERR_UNSUPPORTED_SHAPE;
     if (!E || !dE) return MP_ERR_INVALID_ARG;
-    if (T > 0 && (!X || !target || !loss || !dloss || !dX || !workspace)) return MP_ERR_INVALID_ARG;
-    const void* ptrs[] = {X, E, target, loss, dloss, dX, dE, workspace};
+    if (T > 0 && (!X || !target || !(loss || lse_in) || !dloss || !dX || !workspace)) return MP_ERR_INVALID_ARG;
+    const void* ptrs[] = {X, E, target, loss, lse_in, dloss, dX, dE, workspace};
     for (const void* p : ptrs)
         if (p && !aligned16(p)) return MP_ERR_MISALIGNED;
     if (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)) return MP_ERR_MISALIGNED;
@@ -117,16 +119,20 @@ extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const i
         return cudaMemsetAsync(dE, 0, size_t(v_pad) * h * 2, s) == cudaSuccess ? MP_OK : MP_ERR_CUDA;
     }
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    float* lse = reinterpret_cast<float*>(ws + lay.lse_off);
+    float* lse_ws = reinterpret_cast<float*>(ws + lay.lse_off);
     float* acc = reinterpret_cast<float*>(ws + lay.acc_off);
     __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + lay.dz_off);
     const __nv_bfloat16* Xb = reinterpret_cast<const __nv_bfloat16*>(X);
     const __nv_bfloat16* Eb = reinterpret_cast<const __nv_bfloat16*>(E);
 
-    if (launch_pdl(ce_lse_kernel, dim3(ceil_div(T, 8)), dim3(256), 0, s, Xb, Eb, target, loss, lse, T, h, v_valid,
-                   d_status) != cudaSuccess ||
-        cudaGetLastError() != cudaSuccess)
-        return MP_ERR_CUDA;
+    const float* lse = lse_in;
+    if (lse == nullptr) {
+        if (launch_pdl(ce_lse_kernel, dim3(ceil_div(T, 8)), dim3(256), 0, s, Xb, Eb, target, loss, lse_ws, T, h,
+                       v_valid, d_status) != cudaSuccess ||
+            cudaGetLastError() != cudaSuccess)
+            return MP_ERR_CUDA;
+        lse = lse_ws;
+    }
 
     // Vocabulary chunks of vs columns (whole shards, in shard order): one chunk when the
     // workspace holds every shard's dZ, else one shard at a time.
@@ -207,4 +213,22 @@ extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const i
         if (launch_gemm_tc<256, EPI_ACC, 4>(m12, a12, sms, s) != cudaSuccess) return MP_ERR_CUDA;
     }
     return MP_OK;
+}
+
+extern "C" mp_status mp_vocab_ce_bwd(const mp_bf16* X, const mp_bf16* E, const int32_t* target, const float* loss,
+                                     const float* dloss, mp_bf16* dX, mp_bf16* dE, void* workspace,
+                                     size_t workspace_bytes, int T, int h, int v_pad, int v_valid, int t,
+                                     uint32_t* d_status, void* stream) {
+    if (T > 0 && !loss) return MP_ERR_INVALID_ARG;
+    return ce_bwd(X, E, target, loss, nullptr, dloss, dX, dE, workspace, workspace_bytes, T, h, v_pad, v_valid, t,
+                  d_status, stream);
+}
+
+extern "C" mp_status mp_vocab_ce_bwd_lse(const mp_bf16* X, const mp_bf16* E, const int32_t* target, const float* lse,
+                                         const float* dloss, mp_bf16* dX, mp_bf16* dE, void* workspace,
+                                         size_t workspace_bytes, int T, int h, int v_pad, int v_valid, int t,
+                                         uint32_t* d_status, void* stream) {
+    if (T > 0 && !lse) return MP_ERR_INVALID_ARG;
+    return ce_bwd(X, E, target, nullptr, lse, dloss, dX, dE, workspace, workspace_bytes, T, h, v_pad, v_valid, t,
+                  d_status, stream);
 }
