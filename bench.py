@@ -796,7 +796,11 @@ def main(argv=None):
     if args.profile_case != "none":
         return profile_case(args.profile_case, dev)
     if args.sweep:
-        return run_sweep(dev, max(args.steps // 20, 5), args.warmup)
+        sampler = ClockSampler(physical_gpu(local_rank))
+        sampler.start()
+        rc = run_sweep(dev, max(args.steps // 20, 5), args.warmup)
+        print(json.dumps({"sweep_clocks": sampler.stop()}), flush=True)
+        return rc
 
     step = Step(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)

@@ -164,9 +164,14 @@ MP_API mp_status mp_mlp_bwd_shards(const mp_bf16* X, const mp_bf16* A, const mp_
                             uint32_t* d_status, void* stream);
 
 /*
- * Bytes of workspace mp_vocab_ce needs: fp32 triples [P][3][T], P = the number
- * of vocabulary partitions (the t shards, each cut into equal chunks of whole
- * tiles for load balance). Returns 0 on invalid sizes.
+ * Bytes of workspace mp_vocab_ce needs for its fastest partition: fp32 triples
+ * [P][3][T], P = the number of vocabulary partitions (the t shards, each cut into
+ * equal chunks of whole tiles; the chunk size balances the logit kernel's units
+ * over the GPU for this T, e.g. P = 40 at T = 8192 and 200 at T = 4096 for
+ * v_pad = 51,200, t = 8). A smaller workspace also works down to one partition
+ * per shard (12 t T bytes): the entry points then take the fastest partition
+ * that fits it (mp_vocab_ce_partials and mp_vocab_ce_combine must be given the
+ * same workspace size). Returns 0 on invalid sizes.
  */
 MP_API size_t mp_vocab_ce_workspace_bytes(int T, int v_pad, int t);
 
@@ -180,7 +185,8 @@ MP_API size_t mp_vocab_ce_workspace_bytes(int T, int v_pad, int t);
  *
  *   X [T, h] bf16, E [v_pad, h] bf16 (the vocabulary split into t row blocks of
  *   v_pad / t), target [T] int32 in [0, v_valid), loss [T] fp32 output,
- *   workspace >= mp_vocab_ce_workspace_bytes(T, v_pad, t) bytes (fp32 triples).
+ *   workspace: mp_vocab_ce_workspace_bytes(T, v_pad, t) bytes (fp32 triples), or
+ *   fewer down to 12 t T bytes (a coarser partition; MP_ERR_WORKSPACE below that).
  *   Size rules: h % 64 == 0; t >= 1; v_pad % (128 t) == 0; 1 <= v_valid <= v_pad.
  *   A target outside [0, v_valid) sets MP_DEV_TARGET_RANGE and gives NaN loss for
  *   that token; nothing is read out of bounds.
@@ -300,9 +306,11 @@ MP_API mp_status mp_attn_fwd(const mp_bf16* X, const mp_bf16* Wqkv, const mp_bf1
  * Same inputs, outputs and size rules as mp_vocab_ce, without the workspace: the
  * triples live in a static device array of MP_CE_NOALLOC_MAX_FLOATS floats
  * (4 MiB), held by every GPU the entry point has run on, until exit.
- *   - Problems needing more than that (mp_vocab_ce_workspace_bytes(T, v_pad, t)
- *     > 4 MiB, e.g. T > 8738 at v_pad = 51,200, t = 8) return MP_ERR_WORKSPACE
- *     before any launch.
+ *   - The vocabulary partition is the fastest one whose triples fit in 4 MiB
+ *     (the same as mp_vocab_ce's when mp_vocab_ce_workspace_bytes(T, v_pad, t)
+ *     <= 4 MiB, e.g. T <= 8738 at v_pad = 51,200, t = 8 apart from small T).
+ *     Problems that fit in no partition (one per shard: 12 t T bytes > 4 MiB,
+ *     e.g. T > 43,690 at t = 8) return MP_ERR_WORKSPACE before any launch.
  *   - Nothing is allocated by the call: no cudaMalloc, cudaFree or allocating
  *     library call. CUDA itself places the array on a device when it loads the
  *     code that holds it, which with lazy module loading (the default) is this

@@ -118,11 +118,7 @@ static mp_status check_ce_shape(int T, int h, int v_pad, int v_valid, int t) {
 
 using namespace mptp;
 
-extern "C" size_t mp_vocab_ce_workspace_bytes(int T, int v_pad, int t) {
-    CePlan plan;
-    if (T < 0 || !ce_plan(v_pad, t, &plan)) return 0;
-    return size_t(plan.P) * 3 * size_t(T) * sizeof(float);
-}
+extern "C" size_t mp_vocab_ce_workspace_bytes(int T, int v_pad, int t) { return ce_plan_workspace(T, v_pad, t, 0); }
 
 extern "C" mp_status mp_vocab_ce_partials(const mp_bf16* X, const mp_bf16* E, const int32_t* target,
                                           void* workspace, size_t workspace_bytes, int T, int h, int v_pad,
@@ -134,11 +130,12 @@ extern "C" mp_status mp_vocab_ce_partials(const mp_bf16* X, const mp_bf16* E, co
     if (!aligned16(X) || !aligned16(E) || !aligned16(target) || !aligned16(workspace) ||
         (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)))
         return MP_ERR_MISALIGNED;
-    if (workspace_bytes < mp_vocab_ce_workspace_bytes(T, v_pad, t)) return MP_ERR_WORKSPACE;
+    // The partition follows the workspace given (the preferred plan when it fits).
+    if (workspace_bytes < ce_plan_workspace(T, v_pad, t, workspace_bytes)) return MP_ERR_WORKSPACE;
     int sms = 0;
     if ((st = check_device(&sms)) != MP_OK) return st;
     CePlan plan;
-    ce_plan(v_pad, t, &plan);
+    ce_plan(T, v_pad, t, workspace_bytes, &plan);
 
     TmapSet m{};
     if (!make_tmap_bf16(&m.a, X, h, T, h, 64, BM) || !make_tmap_bf16(&m.b, E, h, v_pad, h, 64, plan.bn / 2))
@@ -174,12 +171,12 @@ static mp_status ce_combine(const void* workspace, size_t workspace_bytes, const
     if (!aligned16(workspace) || !aligned16(target) || !aligned16(loss) || (lse && !aligned16(lse)) ||
         (d_status && (reinterpret_cast<uintptr_t>(d_status) & 3u)))
         return MP_ERR_MISALIGNED;
-    if (workspace_bytes < mp_vocab_ce_workspace_bytes(T, v_pad, t)) return MP_ERR_WORKSPACE;
+    if (workspace_bytes < ce_plan_workspace(T, v_pad, t, workspace_bytes)) return MP_ERR_WORKSPACE;
     int sms = 0;
     mp_status st = check_device(&sms);
     if (st != MP_OK) return st;
     CePlan plan;
-    ce_plan(v_pad, t, &plan);
+    ce_plan(T, v_pad, t, workspace_bytes, &plan);
     const int G = combine_group(T, sms);
     const int W = G == CMB_WARPS ? CMB_WARPS : 4;  // warps per block
     const cudaError_t e = launch_pdl(G > 1 ? ce_combine_kernel<true> : ce_combine_kernel<false>,

@@ -52,8 +52,9 @@ extern "C" mp_status mp_vocab_ce_noalloc(const mp_bf16* X, const mp_bf16* E, con
                                          void* stream) {
     if (T < 0 || h <= 0 || v_pad <= 0 || t < 1 || v_valid < 1) return MP_ERR_INVALID_ARG;
     if (h % 64 != 0 || v_pad % (128 * t) != 0 || v_valid > v_pad) return MP_ERR_UNSUPPORTED_SHAPE;
-    // The triples must fit in the static array; larger problems are refused before any launch.
-    const size_t need = mp_vocab_ce_workspace_bytes(T, v_pad, t);
+    // The triples must fit in the static array (in the partition that fits it best); larger
+    // problems are refused before any launch.
+    const size_t need = mptp::ce_plan_workspace(T, v_pad, t, sizeof(g_ce_scratch));
     if (need > sizeof(g_ce_scratch) || (T > 0 && need == 0)) return MP_ERR_WORKSPACE;
     int sms = 0;
     mp_status st = mptp::check_device(&sms);

@@ -113,22 +113,58 @@ unsigned long long wait_budget_ns() {
     return 2000000000ull;
 }
 
-bool ce_plan(int v_pad, int t, CePlan* plan) {
-    if (t < 1 || v_pad < 128 * t || v_pad % (128 * t) != 0) return false;
+static void ce_plan_with(int v_pad, int t, int tpu, CePlan* plan) {
+    const int vs = v_pad / t;
+    plan->bn = (vs % 256 == 0) ? 256 : 128;
+    plan->tiles_per_unit = tpu;
+    plan->chunk_cols = tpu * plan->bn;
+    plan->P = v_pad / plan->chunk_cols;
+}
+
+static size_t ce_plan_bytes(int T, const CePlan& p) { return size_t(p.P) * 3 * size_t(T) * sizeof(float); }
+
+bool ce_plan(int T, int v_pad, int t, size_t workspace_limit, CePlan* plan) {
+    if (T < 0 || t < 1 || v_pad < 128 * t || v_pad % (128 * t) != 0) return false;
     const int vs = v_pad / t;
     const int bn = (vs % 256 == 0) ? 256 : 128;
-    const int nb = vs / bn;
-    int tpu = nb;
+    const int nb = vs / bn;  // tiles per shard
+    // The default chunk: the smallest divisor of nb that is at least 4 tiles (or the whole shard).
+    int base = nb;
     for (int d = 4; d <= nb; ++d)
         if (nb % d == 0) {
-            tpu = d;
+            base = d;
             break;
         }
-    plan->bn = bn;
-    plan->tiles_per_unit = tpu;
-    plan->chunk_cols = tpu * bn;
-    plan->P = v_pad / plan->chunk_cols;
+    // Estimated time in tile-times on CE_PLAN_PAIRS pairs: rounds of units x tiles per unit.
+    const long long mblocks = (static_cast<long long>(T) + 255) / 256;
+    auto cost = [&](int tpu) {
+        const long long units = mblocks * (v_pad / (tpu * bn));
+        return (units + CE_PLAN_PAIRS - 1) / CE_PLAN_PAIRS * tpu;
+    };
+    // Preferred: the default, or a finer divisor that is at least 3 % cheaper (more partitions
+    // balance the last round of units); fewer tiles per unit only when it pays.
+    int pick = base;
+    for (int d = 1; d < base; ++d)
+        if (nb % d == 0 && cost(d) * 100 <= cost(base) * 97 && cost(d) < cost(pick)) pick = d;
+    ce_plan_with(v_pad, t, pick, plan);
+    if (workspace_limit == 0 || ce_plan_bytes(T, *plan) <= workspace_limit) return true;
+    // A smaller workspace: the cheapest plan that fits, else the one with the fewest partitions.
+    int fit = 0;
+    for (int d = 1; d <= nb; ++d) {
+        if (nb % d != 0) continue;
+        CePlan c;
+        ce_plan_with(v_pad, t, d, &c);
+        if (ce_plan_bytes(T, c) <= workspace_limit && (fit == 0 || cost(d) < cost(fit) || (cost(d) == cost(fit) && d > fit)))
+            fit = d;
+    }
+    ce_plan_with(v_pad, t, fit > 0 ? fit : nb, plan);
     return true;
+}
+
+size_t ce_plan_workspace(int T, int v_pad, int t, size_t workspace_limit) {
+    CePlan plan;
+    if (!ce_plan(T, v_pad, t, workspace_limit, &plan)) return 0;
+    return ce_plan_bytes(T, plan);
 }
 
 namespace {

@@ -51,14 +51,25 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline int ceil_div(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 // Cross-entropy partitioning: each of the t vocabulary shards (v_pad / t rows
-// of E) is cut into equal chunks of whole BN-wide tiles for load balance.
+// of E) is cut into equal chunks of whole BN-wide tiles for load balance; a unit of
+// the logit kernel is one 256-token block times one chunk.
 struct CePlan {
     int bn;              // 256 or 128
     int tiles_per_unit;  // tiles per chunk
     int chunk_cols;      // tiles_per_unit * bn
     int P;               // v_pad / chunk_cols partitions
 };
-bool ce_plan(int v_pad, int t, CePlan* plan);
+// CTA pairs the plan balances the units over: the GB300's 152 SMs hold 76 pairs of the logit
+// kernel. The plan depends on the sizes only (not on the device), so the workspace size and
+// every entry point agree.
+constexpr int CE_PLAN_PAIRS = 76;
+// The plan for T tokens. Chunks of at least four tiles, or fewer tiles when that balances the
+// units' last round at least 3 % better (T = 4096, v_pad = 51,200, t = 8: one-tile chunks,
+// 43 rounds of one tile against 9 rounds of five). With workspace_limit > 0 and the preferred
+// plan's triples larger than it: the cheapest plan that fits (else the fewest partitions).
+bool ce_plan(int T, int v_pad, int t, size_t workspace_limit, CePlan* plan);
+// Bytes of the triples of that plan (0 on invalid sizes).
+size_t ce_plan_workspace(int T, int v_pad, int t, size_t workspace_limit);
 
 // Two extra streams of the current device with fork/join events, for GEMMs that run
 // side by side with the caller's stream; every launch on them is still ordered after

@@ -55,9 +55,13 @@ def test_status_strings(L):
 
 def test_workspace_bytes(L):
     import tensor_transformer_layer_gb300 as mp
-    # 51,200 padded rows, t = 8: shards of 6,400 = 25 tiles of 256, chunks of 5 tiles -> P = 40
+    # 51,200 padded rows, t = 8: shards of 6,400 = 25 tiles of 256. T = 8192: chunks of 5 tiles,
+    # P = 40 (1280 units, 17 rounds on 76 pairs either way). T = 4096: one-tile chunks, P = 200
+    # (3200 units in 43 rounds of one tile, against 640 in 9 rounds of five).
     assert mp.mp_vocab_ce_workspace_bytes(8192, 51200, 8) == 40 * 3 * 8192 * 4
-    assert mp.mp_vocab_ce_workspace_bytes(10, 768, 2) == (768 // 384) * 3 * 10 * 4
+    assert mp.mp_vocab_ce_workspace_bytes(4096, 51200, 8) == 200 * 3 * 4096 * 4
+    # v_pad / t = 384 = 3 tiles of 128: ten tokens run best as 6 one-tile chunks
+    assert mp.mp_vocab_ce_workspace_bytes(10, 768, 2) == 6 * 3 * 10 * 4
     assert mp.mp_vocab_ce_workspace_bytes(10, 1000, 8) == 0     # v_pad not a multiple of 128 t
     assert mp.mp_vocab_ce_workspace_bytes(-1, 1024, 1) == 0
     assert mp.mp_vocab_ce_workspace_bytes(0, 1024, 1) == 0
@@ -139,9 +143,20 @@ def test_no_device_answer(L):
     assert L.mp_mlp_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, 8, 64, 128, 1, None, None) == 4
     assert L.mp_vocab_ce(FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, 4, 64, 256, 200, 1, None, None) == 4
     # The no-allocation entry point: a T = 0 call also reaches the device (it places the static
-    # array there), so without one it answers MP_ERR_NO_DEVICE; too large a problem is refused first.
+    # array there), so without one it answers MP_ERR_NO_DEVICE; a problem whose triples fit the
+    # 4 MiB array in no partition (one per shard: 8 x 3 x 43,691 floats) is refused first.
     assert L.mp_vocab_ce_noalloc(None, None, None, None, 0, 64, 256, 200, 1, None, None) == 4
-    assert L.mp_vocab_ce_noalloc(FAKE, FAKE, FAKE, FAKE, 8739, 64, 51200, 50257, 8, None, None) == 8
+    assert L.mp_vocab_ce_noalloc(FAKE, FAKE, FAKE, FAKE, 43690, 64, 51200, 50257, 8, None, None) == 4
+    assert L.mp_vocab_ce_noalloc(FAKE, FAKE, FAKE, FAKE, 43691, 64, 51200, 50257, 8, None, None) == 8
+    # A smaller workspace than mp_vocab_ce_workspace_bytes runs a coarser partition that fits it
+    # (then the device check answers); none fits: MP_ERR_WORKSPACE before any device call.
+    want = 200 * 3 * 4096 * 4
+    assert L.mp_vocab_ce(FAKE, FAKE, FAKE, FAKE, FAKE, want, 4096, 64, 51200, 50257, 8, None, None) == 4
+    assert L.mp_vocab_ce(FAKE, FAKE, FAKE, FAKE, FAKE, 4 << 20, 4096, 64, 51200, 50257, 8, None, None) == 4
+    assert L.mp_vocab_ce(FAKE, FAKE, FAKE, FAKE, FAKE, 8 * 3 * 4096 * 4, 4096, 64, 51200, 50257, 8, None,
+                         None) == 4
+    assert L.mp_vocab_ce(FAKE, FAKE, FAKE, FAKE, FAKE, 8 * 3 * 4096 * 4 - 4, 4096, 64, 51200, 50257, 8, None,
+                         None) == 8
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

@@ -52,6 +52,28 @@ def test_ce_8p3b_layer_sampled():
     assert np.all(np.isfinite(got))
 
 
+def test_ce_partition_follows_workspace():
+    # T = 4096 runs one-tile vocabulary chunks (200 partitions) with the workspace
+    # mp_vocab_ce_workspace_bytes asks for, and coarser ones in a smaller workspace (40 partitions
+    # in 4 MiB, 8 in 8 x 3 x T floats): the same loss within fp32 rounding, and the oracle's.
+    import tensor_transformer_layer_gb300 as m
+    T, h, v_pad, v_valid, t = 4096, 128, 51200, 50257, 8
+    inp = synth.ce_inputs(T, h, v_pad, v_valid, seed=4500)
+    X, E, tgt = inp["X"].cuda(), inp["E"].cuda(), inp["target"].cuda()
+    out = []
+    for nbytes in (m.mp_vocab_ce_workspace_bytes(T, v_pad, t), 4 << 20, 8 * 3 * T * 4):
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        loss = torch.empty(T, dtype=torch.float32, device="cuda")
+        m.mp_vocab_ce(X, E, tgt, loss, ws, v_valid=v_valid, t=t)
+        torch.cuda.synchronize()
+        out.append(loss.cpu().numpy().astype(np.float64))
+    assert np.max(np.abs(out[1] - out[0])) <= 1e-4 and np.max(np.abs(out[2] - out[0])) <= 1e-4
+    rows = synth.sample_indices(T, 64, seed=23).numpy()
+    want = oracle.ce_loss(f64(inp["X"])[rows], f64(inp["E"]), inp["target"].numpy()[rows], v_valid)
+    for o in out:
+        assert np.max(np.abs(o[rows] - want)) <= LOSS_ABS
+
+
 def test_ce_zero_embedding_closed_form():
     inp = synth.ce_inputs(200, 128, 51200, 50257, seed=4100)
     inp["E"] = torch.zeros_like(inp["E"])

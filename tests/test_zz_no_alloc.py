@@ -75,8 +75,9 @@ def test_noalloc_matches_workspace_entry_point_and_oracle():
 
 def test_noalloc_refuses_problems_beyond_the_array():
     mp, L = _lib()
-    T, h, v_pad, t = 8739, 64, 51200, 8     # 40 partitions x 3 x 8739 floats > 4 MiB
-    assert mp.mp_vocab_ce_workspace_bytes(T, v_pad, t) > 4 * 1024 * 1024
+    # 43,691 tokens: even one vocabulary partition per shard (8 x 3 x T floats) exceeds 4 MiB.
+    T, h, v_pad, t = 43691, 64, 51200, 8
+    assert 8 * 3 * T * 4 > 4 * 1024 * 1024 >= 8 * 3 * (T - 1) * 4
     X = torch.zeros(T, h, dtype=torch.bfloat16, device="cuda")
     E = torch.zeros(v_pad, h, dtype=torch.bfloat16, device="cuda")
     tgt = torch.zeros(T, dtype=torch.int32, device="cuda")
