@@ -771,7 +771,8 @@ def main(argv=None):
                     help="skip the PyTorch/cuBLAS composition timed beside the step for context")
     ap.add_argument("--sweep", action="store_true",
                     help="time MLP fwd+bwd and the fused CE at every point of the layer sweep (one JSON line each)")
-    ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "ce_8p3b", "mlp", "mlp_small", "attn"),
+    ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "ce_8p3b", "mlp", "mlp_small", "mlp_split",
+                                               "attn"),
                     default="none",
                     help="run only a small case of one entry point a few times (for ncu), print nothing")
     args = ap.parse_args(argv)
@@ -948,8 +949,9 @@ def run_sweep(dev, reps, warmup):
 def profile_case(which, dev):
     """Cases for ncu captures: 'ce' (T=2048), 'ce_8p3b' (T=4096, h=3072: 0.35 GB) and 'mlp' (the 8.3B
     layer, 0.7 GB) are small enough for multi-pass captures (under 1 GB on the device, 0.2-0.7 ms
-    kernels, inputs > L2); 'mlp_small' is the sweep's T = 2048, h = 1536 point; 'ce_full' is the bench's
-    CE launch, for one-pass metrics only."""
+    kernels, inputs > L2); 'mlp_small' is the sweep's T = 2048, h = 1536 point and 'mlp_split' its
+    T = 2048, h = 3072 point (K2 on the split-K kernel); 'ce_full' is the bench's CE launch, for
+    one-pass metrics only."""
     import torch
 
     import synth
@@ -980,6 +982,8 @@ def profile_case(which, dev):
         T, h, f, t = MLP["T"], MLP["h"], MLP["f"], MLP["t"]
         if which == "mlp_small":   # the sweep's smallest point: T = 2048, h = 1536
             T, h, f = 2048, 1536, 6144
+        if which == "mlp_split":   # T = 2048, h = 3072: the row-parallel GEMM split over two pairs
+            T, h, f = 2048, 3072, 12288
         mi = synth.mlp_inputs(T, h, f, seed=MLP["seed"])
         d = {k: v.to(dev) for k, v in mi.items()}
         e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=dev)
