@@ -186,3 +186,24 @@ def test_backward_empty_batch_range():
     dA, dB = dA.cpu(), dB.cpu()
     assert torch.all(dA[:, 64:192] == 0) and torch.all(dA[:, :64] == SENTINEL) and torch.all(dA[:, 192:] == SENTINEL)
     assert torch.all(dB[64:192] == 0) and torch.all(dB[:64] == SENTINEL) and torch.all(dB[192:] == SENTINEL)
+
+
+def test_8p3b_layer_single_shard_partials_sampled():
+    # T = 4096, h = 3072, f = 12288, t = 8 (the bench's layer): shard 5's partial output Z_5 and its
+    # part of dX on sampled rows, against the shard-by-shard formulas of the oracle module restricted
+    # to those rows (a row of Z_i or dX_i needs only its own rows of X and dZ).
+    w = synth.WORKLOADS["mlp_8p3b"]
+    T, h, f, t = w["T"], w["h"], w["f"], w["t"]
+    i, fs = 5, f // t
+    inp = synth.mlp_inputs(T, h, f, w["seed"])
+    fwd = _fwd_range(inp, t, i, 1)
+    dev = run_mlp_fwd(inp, t)
+    g = _bwd_range(dev, inp["dZ"], t, i, 1)
+    rows = synth.sample_indices(T, 64, seed=51).numpy()
+    X, A, B, G = (f64(inp[k]) for k in ("X", "A", "B", "dZ"))
+    Ai, Bi = A[:, i * fs:(i + 1) * fs], B[i * fs:(i + 1) * fs, :]
+    Ui = X[rows] @ Ai
+    Zi = oracle.gelu(Ui) @ Bi
+    dXi = ((G[rows] @ Bi.T) * oracle.gelu_prime(Ui)) @ Ai.T
+    assert rel_fro(f64(fwd["Z"])[rows], Zi) <= Z_REL_FRO and max_abs(f64(fwd["Z"])[rows], Zi) <= Z_MAX_ABS
+    assert rel_fro(f64(g["dX"])[rows], dXi) <= GRAD_REL_FRO

@@ -21,6 +21,7 @@ pytestmark = pytest.mark.gpu
     (300, 192, 3072, 4),     # ragged T, N = h narrower than one tile; 48 K blocks over the pairs
     (256, 768, 3072, 2),     # the tiny workload
     (513, 320, 2560, 5),     # ragged T and N; shards of 512 columns
+    (300, 192, 2112, 3),     # 33 K blocks: the two pairs run 16 and 17
 ])
 def test_split_forward_matches_oracle(T, h, f, t):
     inp = synth.mlp_inputs(T, h, f, 8000 + T, with_grad=False)
