@@ -792,7 +792,12 @@ def main(argv=None):
     torch.cuda.set_device(dev)
 
     from tensor_transformer_layer_gb300 import build as _build
-    _build.build()
+    # One rank compiles (when the library is missing or stale); the others wait, then load it.
+    if rank == 0:
+        _build.build()
+    barrier(world)
+    if rank != 0:
+        _build.build()
 
     if args.profile_case != "none":
         return profile_case(args.profile_case, dev)
