@@ -10,7 +10,9 @@
 //        per-token log-sum-exp, so only one shard of logit gradients exists at a time;
 //   K11  dE_i = dZ_i^T X  (both operands MN-major);
 //   K12  dX += dZ_i E_i   (fp32 accumulation across shards in shard order - the sum the
-//        forward's all-reduce would carry - and one bf16 store after the last shard).
+//        forward's all-reduce would carry: shard 0's tiles are stored, later shards' tiles
+//        added at L2 by TMA reductions, and the last shard adds the accumulator in registers
+//        and stores bf16).
 // The log-sum-exp comes from the forward: either exported by it (mp_vocab_ce_lse, then
 // mp_vocab_ce_bwd_lse), or rebuilt from its loss: lse = loss + z_target, with z_target
 // = X[r] . E[target[r]] recomputed in fp32 (K9, mp_vocab_ce_bwd).
@@ -192,7 +194,7 @@ static mp_status ce_bwd(const mp_bf16* X, const mp_bf16* E, const int32_t* targe
         TmapSet m12{};
         int b12f = 0;
         if (!make_tmap_bf16(&m12.a, dz, vs, T, vs, 64, BM) || !(b12f = make_tmap_mn_operand(&m12.b, Ei, h, vs, h)) ||
-            !make_tmap_bf16_out(&m12.o0, dX, h, T, h))
+            !make_tmap_bf16_out(&m12.o0, dX, h, T, h) || (C > 1 && !make_tmap_f32_out(&m12.o1, acc, h, T, h)))
             return MP_ERR_CUDA;
         GemmArgs a12{};
         a12.pr.M = T;

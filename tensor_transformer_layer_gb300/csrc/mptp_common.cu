@@ -73,6 +73,19 @@ bool make_tmap_bf16_out(CUtensorMap* map, const void* base, uint64_t inner, uint
     return make_tmap_bf16_sw(map, base, inner, outer, pitch_elems, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+bool make_tmap_f32_out(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch_elems * 4};
+    cuuint32_t box[2] = {32, 32};  // 32 rows of 128 bytes
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 mp_status check_device(int* num_sms) {
     constexpr int MAXDEV = 64;
     static std::atomic<int> cached[MAXDEV];  // 0 unknown, -1 bad, >0 SM count

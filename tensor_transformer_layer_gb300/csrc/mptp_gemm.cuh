@@ -72,12 +72,13 @@ enum EpiKind : int {
     EPI_DGELU = 2,  // o0 = bf16(acc * GeLU'(aux)), aux = bf16 U
     EPI_CE = 3,     // per-row online max / sum-exp / target logit over the unit
     EPI_DZ = 4,     // o0 = bf16(dloss * (exp(acc - lse) - [col == target])), 0 on padding columns
-    EPI_ACC = 5,    // fp32 accumulation across launches into `acc`; the last launch stores bf16 o0
+    EPI_ACC = 5,    // fp32 accumulation across launches into `acc` (tensor map o1); the last launch
+                    // stores bf16 o0
 };
 
 enum AccMode : int {
-    ACC_FIRST = 0,  // acc = C
-    ACC_MID = 1,    // acc += C
+    ACC_FIRST = 0,  // acc = C          (TMA store of fp32 boxes through o1)
+    ACC_MID = 1,    // acc += C         (TMA reduction: the add is done at L2, no read back)
     ACC_LAST = 2,   // o0 = bf16(acc + C)
     ACC_ONLY = 3,   // o0 = bf16(C)
 };
@@ -135,7 +136,9 @@ struct GemmCfg {
     static constexpr int B_BYTES = BNH * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr uint32_t TMEM_COLS = BN <= 128 ? 256 : 512;  // two accumulators, power of two
-    static constexpr int STG_BYTES = EPI == EPI_CE ? 0 : NE * STG_BYTES_PER_WARP;
+    // staging per epilogue warp: two 32 x 32 boxes, bf16 (2 KB each) or, accumulating, fp32 (4 KB)
+    static constexpr int STG_PER_WARP = EPI == EPI_ACC ? 2 * 4096 : STG_BYTES_PER_WARP;
+    static constexpr int STG_BYTES = EPI == EPI_CE ? 0 : NE * STG_PER_WARP;
     static constexpr int MAX_STAGES = 8;
     static constexpr int FIT_STAGES = static_cast<int>((SMEM_LIMIT - 1024 - 512 - STG_BYTES) / STAGE_BYTES);
     static constexpr int STAGES = FIT_STAGES < MAX_STAGES ? FIT_STAGES : MAX_STAGES;
@@ -276,6 +279,30 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap* map, uint8_t*
     sbuf ^= 1;
 }
 
+// The fp32 form: 32 rows x 32 columns (128-byte rows, 16-byte chunk j of row r at chunk
+// j ^ (r & 7), the 128-byte swizzle) in one of the warp's two 4 KB boxes, then lane 0 either
+// stores the box or adds it into global memory with a TMA reduction.
+__device__ __forceinline__ void stage_and_store_f32(const CUtensorMap* map, uint8_t* stg, int& sbuf, int lane,
+                                                    const uint32_t (&v)[32], int x, int y, bool add) {
+    if (lane == 0) bulk_wait_group_read<1>();
+    __syncwarp();
+    uint8_t* row = stg + sbuf * 4096 + lane * 128;
+    const int sw = lane & 7;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<uint4*>(row + ((j ^ sw) << 4)) = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (add)
+            tma_reduce_add_2d(map, stg + sbuf * 4096, x, y);
+        else
+            tma_store_2d(map, stg + sbuf * 4096, x, y);
+        bulk_commit_group();
+    }
+    sbuf ^= 1;
+}
+
 __device__ __forceinline__ void decode_unit(const ProbInfo& p, int lu, int& m_blk, int& ucol) {
     if (p.n_fastest) {
         const int ncols = p.num_units / p.num_m_blocks;
@@ -333,7 +360,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
         prefetch_tensormap(&maps.a);
         prefetch_tensormap(&maps.b);
         if (EPI != EPI_CE) prefetch_tensormap(&maps.o0);
-        if (EPI == EPI_GELU && args.has_out1) prefetch_tensormap(&maps.o1);
+        if ((EPI == EPI_GELU && args.has_out1) || (EPI == EPI_ACC && args.acc_mode <= ACC_MID))
+            prefetch_tensormap(&maps.o1);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
@@ -471,7 +499,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
         const int q = warp & 3;                      // TMEM lane quarter this warp may access
         const int c_begin = (e >> 2) * MY_CHUNKS;    // column half (8 warps) or all columns (4)
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-        uint8_t* stg = stg_base + e * STG_BYTES_PER_WARP;
+        uint8_t* stg = stg_base + e * Cfg::STG_PER_WARP;
         int sbuf = 0;
         uint32_t tcount = 0;
         bool ok = true;
@@ -609,21 +637,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GemmCfg<BN, EPI, NE>
 #pragma unroll
                             for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
                             stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
-                        } else if (row_ok) {
-                            float4* dst = reinterpret_cast<float4*>(args.acc + row * args.ld_acc + col0);
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                float4 c4 = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                                if (args.acc_mode == ACC_MID) {
-                                    const float4 a4 = dst[j];
-                                    c4.x += a4.x;
-                                    c4.y += a4.y;
-                                    c4.z += a4.z;
-                                    c4.w += a4.w;
-                                }
-                                dst[j] = c4;
-                            }
+                        } else {
+                            stage_and_store_f32(&maps.o1, stg, sbuf, lane, r, col0, row0, args.acc_mode == ACC_MID);
                         }
                     } else {  // EPI_CE
                         const int lim = args.v_valid - col0;  // valid columns in this chunk

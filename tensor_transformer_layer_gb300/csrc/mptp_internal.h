@@ -34,6 +34,9 @@ bool make_tmap_bf16_mn3d(CUtensorMap* map, const void* base, uint64_t inner, uin
 // per stage), else 64-wide 2-D boxes (flag 1). 0: the map could not be encoded.
 int make_tmap_mn_operand(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems);
 bool make_tmap_bf16_out(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems);
+// fp32 epilogue target [outer rows, inner columns] in 32 x 32 boxes (128-byte rows, 128-byte
+// swizzle): the staging layout of the accumulating epilogue's TMA stores and reductions.
+bool make_tmap_f32_out(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_elems);
 
 // Unit order for a GEMM whose A operand (M side) has a_bytes and B operand (N side)
 // b_bytes: walk the smaller operand's blocks fastest, so it stays resident in L2

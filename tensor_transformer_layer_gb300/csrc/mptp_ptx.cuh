@@ -125,6 +125,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
         "r"(smem_u32(src)), "r"(x), "r"(y)
         : "memory");
 }
+// TMA tiled reduction: global[box at (x, y)] += shared box, element by element (the element
+// type and the add come from the tensor map; fp32 adds round to nearest even).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until at most N committed bulk groups of this thread still read shared memory.
 template <int N>
