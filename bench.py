@@ -771,8 +771,8 @@ def main(argv=None):
                     help="skip the PyTorch/cuBLAS composition timed beside the step for context")
     ap.add_argument("--sweep", action="store_true",
                     help="time MLP fwd+bwd and the fused CE at every point of the layer sweep (one JSON line each)")
-    ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "ce_8p3b", "mlp", "mlp_small", "mlp_split",
-                                               "attn"),
+    ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "ce_8p3b", "ce_bwd", "mlp", "mlp_small",
+                                               "mlp_split", "attn"),
                     default="none",
                     help="run only a small case of one entry point a few times (for ncu), print nothing")
     args = ap.parse_args(argv)
@@ -956,7 +956,9 @@ def profile_case(which, dev):
     layer, 0.7 GB) are small enough for multi-pass captures (under 1 GB on the device, 0.2-0.7 ms
     kernels, inputs > L2); 'mlp_small' is the sweep's T = 2048, h = 1536 point and 'mlp_split' its
     T = 2048, h = 3072 point (K2 on the split-K kernel); 'ce_full' is the bench's CE launch, for
-    one-pass metrics only."""
+    one-pass metrics only; 'ce_bwd' is the CE backward on the bench's CE workload from the exported
+    log-sum-exp, one call shard by shard and then one call in one pass (1.3 GB on the device; for
+    the one-pass launch list)."""
     import torch
 
     import synth
@@ -971,6 +973,23 @@ def profile_case(which, dev):
         for _ in range(3):
             mp.mp_attn_fwd(X, Wqkv, Wo, out, QKV, O, b=b, s=s_, heads=heads, t=t)
         torch.cuda.synchronize()
+        return 0
+    if which == "ce_bwd":
+        T, h, v_pad, v_valid, t = CE["T"], CE["h"], CE["v_pad"], CE["v_valid"], CE["t"]
+        ci = synth.ce_inputs(T, h, v_pad, v_valid, seed=CE["seed"])
+        X, E, tgt = ci["X"].to(dev), ci["E"].to(dev), ci["target"].to(dev)
+        ws = torch.empty(mp.mp_vocab_ce_workspace_bytes(T, v_pad, t), dtype=torch.uint8, device=dev)
+        loss = torch.empty(T, dtype=torch.float32, device=dev)
+        lse = torch.empty_like(loss)
+        mp.mp_vocab_ce_lse(X, E, tgt, loss, lse, ws, v_valid=v_valid, t=t)
+        dl = torch.full((T,), 1.0 / T, dtype=torch.float32, device=dev)
+        dX = torch.empty(T, h, dtype=torch.bfloat16, device=dev)
+        dE = torch.empty(v_pad, h, dtype=torch.bfloat16, device=dev)
+        for size in (mp.mp_vocab_ce_bwd_workspace_bytes, mp.mp_vocab_ce_bwd_workspace_bytes_one_pass):
+            wsb = torch.empty(size(T, h, v_pad, t), dtype=torch.uint8, device=dev)
+            mp.mp_vocab_ce_bwd_lse(X, E, tgt, lse, dl, dX, dE, wsb, v_valid=v_valid, t=t)
+            torch.cuda.synchronize()
+            del wsb
         return 0
     if which in ("ce", "ce_full", "ce_8p3b"):
         T, h, v_pad, v_valid, t = (2048 if which == "ce" else CE["T"]), 1536, 51200, 50257, 8
