@@ -563,6 +563,7 @@ def time_next_rows(step, reps, flush):
     attn = {"ms": ams, "tflops": attn_flop / (ams * 1e-3) / 1e12, "flop": attn_flop,
             "shape": [ab, as_, ah, aheads, hd, at],
             "flop_note": "shape b,s,h,heads,d,t; QKV 6Th^2 + causal 4*b*heads*d*s(s+1)/2 + out 2Th^2"}
+    attn.update(time_torch_attn(ax, awqkv, awo, ab, as_, aheads, reps, flush, attn_flop))
     algo = 4.0 * T * h * v_pad      # dX = dZ E and dE = dZ^T X
     executed = 6.0 * T * h * v_pad  # plus the logit recompute (logits are never stored)
     return {"ce_bwd": {"ms": ms, "tflops_algorithmic": algo / (ms * 1e-3) / 1e12,
@@ -572,6 +573,31 @@ def time_next_rows(step, reps, flush):
                                     "executed adds the 2Thv logit recompute"},
             "vocab_embed": embed,
             "attn_fwd": attn}
+
+
+def time_torch_attn(X, Wqkv, Wo, b, s, heads, reps, flush, flop):
+    """Context for the attention block (never part of `value`): the same block composed from
+    PyTorch, X Wqkv and O Wo on cuBLAS and causal scaled_dot_product_attention on its cuDNN
+    backend, on the same device tensors."""
+    import torch
+    import torch.nn.functional as F
+    T, h = X.shape
+    d = h // heads
+    try:
+        from torch.nn.attention import SDPBackend, sdpa_kernel
+
+        def block():
+            qkv = X @ Wqkv
+            q, k, v = (qkv[:, i * h:(i + 1) * h].view(b, s, heads, d).transpose(1, 2) for i in range(3))
+            with sdpa_kernel([SDPBackend.CUDNN_ATTENTION]):
+                o = F.scaled_dot_product_attention(q, k, v, is_causal=True)
+            return o.transpose(1, 2).reshape(T, h) @ Wo
+        block()
+        ms = event_median(block, reps, flush)
+    except Exception as exc:  # a PyTorch without the cuDNN attention backend
+        return {"torch_block": "unavailable: " + str(exc).splitlines()[0][:100]}
+    return {"torch_block_ms": ms, "torch_block_tflops": flop / (ms * 1e-3) / 1e12,
+            "torch_block_note": "PyTorch: X@Wqkv, F.scaled_dot_product_attention(is_causal) on cuDNN, O@Wo"}
 
 
 def time_torch_context(step, reps, flush):
