@@ -63,8 +63,8 @@ struct AttnCfg {
     static_assert(128 * REGS_CTRL + 256 * REGS_SOFTMAX <= ATT_THREADS * 168, "register split");
     static constexpr int KST = D == 64 ? 4 : 3;           // K ring stages
     static constexpr int VST = D == 64 ? 4 : 3;           // V ring stages
-    // q_full, K ring, V ring, s_full/p_full/o_full per query tile, drain
-    static constexpr int NUM_BARS = 1 + 2 * KST + 2 * VST + 2 * 3 + 1;
+    // q_full per query tile, K ring, V ring, s_full/p_full/o_full per query tile, drain
+    static constexpr int NUM_BARS = 2 + 2 * KST + 2 * VST + 2 * 3 + 1;
     static constexpr size_t SMEM_BYTES = 1024 + 2 * Q_BYTES + (KST + VST) * KV_TILE_BYTES + 8 * NUM_BARS + 16;
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory per block");
     // S_A, S_B: 128 columns each (P_g, bf16, overwrites the first 64 columns of S_g);
@@ -94,8 +94,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
     uint8_t* sK = sQ + 2 * Cfg::Q_BYTES;                   // K stage st at st * KV_TILE_BYTES
     uint8_t* sV = sK + KST * Cfg::KV_TILE_BYTES;           // V stage st at st * KV_TILE_BYTES
     uint64_t* bars = reinterpret_cast<uint64_t*>(sV + VST * Cfg::KV_TILE_BYTES);
-    uint64_t* q_full = bars;
-    uint64_t* k_full = bars + 1;
+    uint64_t* q_full = bars;  // [2]: query tile g landed
+    uint64_t* k_full = bars + 2;
     uint64_t* k_empty = k_full + KST;
     uint64_t* v_full = k_empty + KST;
     uint64_t* v_empty = v_full + VST;
@@ -132,7 +132,8 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                         row_base + j * ATT_BKV);
     };
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
+        mbar_init(&q_full[0], 1);
+        mbar_init(&q_full[1], 1);
         mbar_init(drain_bar, 1);
         for (int i = 0; i < KST; ++i) {
             mbar_init(&k_full[i], 1);
@@ -150,19 +151,20 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
         *abort_flag = 0u;
         fence_mbarrier_init();
         fence_proxy_async_smem();
-        // The producer thread issues the first loads (both Q tiles and the first LEAD K tiles,
-        // whose ring stages are still free) now, so that their latency overlaps the rest of the
-        // set-up; QKV is read only once the grid that writes it has completed.
+        // The producer thread issues the first loads (K tile 0, the Q tiles, then the next LEAD - 1
+        // K tiles, whose ring stages are still free) now, so that their latency overlaps the rest
+        // of the set-up; QKV is read only once the grid that writes it has completed. Each Q tile
+        // has a barrier of its own, so S_A(0) starts as soon as K_0 and Q_A have landed.
         prefetch_tensormap(&tmQKV);
         grid_dependency_wait();
-        mbar_arrive_expect_tx(q_full, (has_b ? 2 : 1) * Cfg::Q_BYTES);
-        for (int c = 0; c < NB; ++c)
-            tma_load_2d(sQ + c * Cfg::BOX_BYTES, &tmQKV, q_full, head * D + c * 32, row_base + qt_a * ATT_BQ);
-        if (has_b)
+        issue_kv(0, 1, k_full, sK, 0);
+        for (int g = 0; g < (has_b ? 2 : 1); ++g) {
+            mbar_arrive_expect_tx(&q_full[g], Cfg::Q_BYTES);
             for (int c = 0; c < NB; ++c)
-                tma_load_2d(sQ + Cfg::Q_BYTES + c * Cfg::BOX_BYTES, &tmQKV, q_full, head * D + c * 32,
-                            row_base + qt_b * ATT_BQ);
-        for (int j = 0; j < LEAD && j < n; ++j) issue_kv(j, 1, k_full, sK, j);
+                tma_load_2d(sQ + g * Cfg::Q_BYTES + c * Cfg::BOX_BYTES, &tmQKV, &q_full[g], head * D + c * 32,
+                            row_base + (g ? qt_b : qt_a) * ATT_BQ);
+        }
+        for (int j = 1; j < LEAD && j < n; ++j) issue_kv(j, 1, k_full, sK, j);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
@@ -234,11 +236,17 @@ __global__ void __launch_bounds__(ATT_THREADS, 1)
                 for (int k = 0; k < ATT_BKV / 16; ++k)
                     umma_bf16_ts_elect(d_tmem, a_tmem + k * 8, vd + ((k * 1024) >> 4), IDESC_PV, k > 0 ? 1u : acc0);
             };
-            bool ok = wait_all(q_full, 0) && wait_all(&k_full[0], 0);
+            bool ok = wait_all(&k_full[0], 0) && wait_all(&q_full[0], 0);
             if (ok) {
                 tc_fence_after();
                 s_mma(0, 0);
-                if (has_b) s_mma(1, 0);
+                if (has_b) {
+                    ok = wait_all(&q_full[1], 0);
+                    if (ok) {
+                        tc_fence_after();
+                        s_mma(1, 0);
+                    }
+                }
                 umma_commit_elect(&k_empty[0]);
             }
             for (int j = 0; j < n && ok; ++j) {
