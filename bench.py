@@ -855,16 +855,7 @@ def main(argv=None):
     ms_per_step = total_ms / args.steps
     value = world * step_flop() * args.steps / (total_ms * 1e-3) / 1e12
 
-    breakdown = time_breakdown(step, 9, flush)
-    next_rows = None if args.no_next_rows else time_next_rows(step, 9, flush)
-    context = None if args.no_context else time_torch_context(step, 9, flush)
-    peaks, peak_src = load_peaks()
-    ce_avg_ms = sum(ce_ms) / len(ce_ms)
-    ce_achieved = ce_flop() / (ce_avg_ms * 1e-3) / 1e12
-    traffic = profiled_traffic()
-    mlp_ms = breakdown["mlp_fwd"] + breakdown["mlp_bwd"]
-    ce_call_ms = breakdown["ce_partials"] + breakdown["ce_combine"]
-
+    # The end-to-end leg right after the device-timed steps, in the same thermal state.
     e2e = e2e_all = None
     if not args.no_e2e:
         pipe = "double-buffered: H2D of step i+1 and D2H of step i-1 overlap step i's compute"
@@ -878,6 +869,16 @@ def main(argv=None):
         all_ms = max_over_ranks(all_ms, world, dev)
         e2e_all = {"value": world * step_flop() / (all_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                    "ms_per_step": all_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    breakdown = time_breakdown(step, 9, flush)
+    next_rows = None if args.no_next_rows else time_next_rows(step, 9, flush)
+    context = None if args.no_context else time_torch_context(step, 9, flush)
+    peaks, peak_src = load_peaks()
+    ce_avg_ms = sum(ce_ms) / len(ce_ms)
+    ce_achieved = ce_flop() / (ce_avg_ms * 1e-3) / 1e12
+    traffic = profiled_traffic()
+    mlp_ms = breakdown["mlp_fwd"] + breakdown["mlp_bwd"]
+    ce_call_ms = breakdown["ce_partials"] + breakdown["ce_combine"]
+
     step.check_status()
     sustained = None if args.no_sustained else time_sustained(step, dev, physical_gpu(local_rank))
     ce83 = None if args.no_next_rows else time_ce_8p3b(dev, 9, flush)
