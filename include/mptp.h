@@ -164,6 +164,44 @@ MP_API mp_status mp_mlp_bwd_shards(const mp_bf16* X, const mp_bf16* A, const mp_
                             uint32_t* d_status, void* stream);
 
 /*
+ * The MLP block with each direction in ONE kernel launch: the same computations
+ * as mp_mlp_fwd_shards / mp_mlp_bwd_shards (same arguments, same outputs, equal
+ * bit for bit), scheduled differently. In the forward, the row-parallel GEMM
+ * (Z = sum_i Y_i B_i) starts on a block of 256 tokens as soon as the
+ * column-parallel GEMM has written the columns of Y it reads next; in the
+ * backward, dX (the f sum), dA and dB start as soon as the dU columns they read
+ * exist, on whichever SMs are free. This is the overlap the method describes
+ * between the backward all-reduce and the weight-gradient GEMMs ("Tensor and
+ * pipeline parallelism, and choosing a layout", section 3, the remarks after the
+ * Proposition), inside one grid, and it removes the part-empty last wave and the
+ * ramp of every GEMM but the last.
+ *
+ *   workspace: mp_mlp_fused_workspace_bytes(T, h, f, t) bytes of device memory,
+ *     16-byte aligned, ZERO-FILLED before its first use (e.g. cudaMemset once).
+ *     It holds a few control words and one completion counter per 256-token row
+ *     block and per 256-column tile of Y (dU). Every call returns it to zeros when
+ *     its kernel ends, also after a timeout, so consecutive calls on one stream may
+ *     share it; calls that can run at the same time on the GPU (different streams)
+ *     need a workspace each.
+ *     Smaller, NULL or misaligned: MP_ERR_WORKSPACE, nothing launched.
+ *   Size rules, shard range and outputs as mp_mlp_fwd_shards / mp_mlp_bwd_shards;
+ *   dU_ws as mp_mlp_bwd. T = 0: nothing to compute (the backward zeroes its dA and
+ *   dB range, as mp_mlp_bwd_shards does) and the workspace is not touched.
+ */
+MP_API size_t mp_mlp_fused_workspace_bytes(int T, int h, int f, int t);
+MP_API mp_status mp_mlp_fwd_fused(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B,
+                           mp_bf16* Z, mp_bf16* Y, mp_bf16* U_save,
+                           int T, int h, int f, int t, int shard_begin, int shard_count,
+                           void* workspace, size_t workspace_bytes,
+                           uint32_t* d_status, void* stream);
+MP_API mp_status mp_mlp_bwd_fused(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B,
+                           const mp_bf16* U, const mp_bf16* Y, const mp_bf16* dZ,
+                           mp_bf16* dX, mp_bf16* dA, mp_bf16* dB, mp_bf16* dU_ws,
+                           int T, int h, int f, int t, int shard_begin, int shard_count,
+                           void* workspace, size_t workspace_bytes,
+                           uint32_t* d_status, void* stream);
+
+/*
  * Bytes of workspace mp_vocab_ce needs for its fastest partition: fp32 triples
  * [P][3][T], P = the number of vocabulary partitions (the t shards, each cut into
  * equal chunks of whole tiles; the chunk size balances the logit kernel's units

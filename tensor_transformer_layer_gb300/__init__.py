@@ -10,6 +10,8 @@ Shapes (row-major, contiguous):
   mp_mlp_fwd(X[T,h], A[h,f], B[f,h], Z[T,h], Y[T,f], U_save[T,f] | None, t)
   mp_mlp_bwd(X, A, B, U[T,f], Y[T,f], dZ[T,h], dX[T,h], dA[h,f], dB[f,h], dU_ws[T,f], t)
   mp_mlp_fwd_shards / mp_mlp_bwd_shards: the same with shard_begin, shard_count
+  mp_mlp_fwd_fused / mp_mlp_bwd_fused: the same, one launch per direction, with a zeroed
+      uint8 workspace of mp_mlp_fused_workspace_bytes(T, h, f, t) bytes
   mp_vocab_ce(X[T,h], E[v_pad,h], target[T] int32, loss[T] fp32, workspace uint8, v_valid, t)
 """
 from __future__ import annotations
@@ -31,7 +33,8 @@ STATUS_NAMES = {
     8: "MP_ERR_WORKSPACE",
 }
 # Every symbol include/mptp.h declares.
-EXPORTS = ("mp_mlp_fwd", "mp_mlp_bwd", "mp_mlp_fwd_shards", "mp_mlp_bwd_shards", "mp_vocab_ce_workspace_bytes", "mp_vocab_ce", "mp_vocab_ce_partials",
+EXPORTS = ("mp_mlp_fwd", "mp_mlp_bwd", "mp_mlp_fwd_shards", "mp_mlp_bwd_shards", "mp_mlp_fused_workspace_bytes",
+           "mp_mlp_fwd_fused", "mp_mlp_bwd_fused", "mp_vocab_ce_workspace_bytes", "mp_vocab_ce", "mp_vocab_ce_partials",
            "mp_vocab_ce_combine", "mp_status_string", "mp_status_from_device", "mp_version",
            "mp_vocab_ce_noalloc", "mp_vocab_ce_bwd_workspace_bytes", "mp_vocab_ce_bwd_workspace_bytes_one_pass",
            "mp_vocab_ce_bwd", "mp_vocab_ce_lse", "mp_vocab_ce_bwd_lse", "mp_vocab_embed",
@@ -65,6 +68,12 @@ def lib() -> ctypes.CDLL:
         L.mp_mlp_fwd_shards.restype = _I
         L.mp_mlp_bwd_shards.argtypes = [_P] * 10 + [_I, _I, _I, _I, _I, _I, _P, _P]
         L.mp_mlp_bwd_shards.restype = _I
+        L.mp_mlp_fused_workspace_bytes.argtypes = [_I, _I, _I, _I]
+        L.mp_mlp_fused_workspace_bytes.restype = ctypes.c_size_t
+        L.mp_mlp_fwd_fused.argtypes = [_P] * 6 + [_I] * 6 + [_P, ctypes.c_size_t, _P, _P]
+        L.mp_mlp_fwd_fused.restype = _I
+        L.mp_mlp_bwd_fused.argtypes = [_P] * 10 + [_I] * 6 + [_P, ctypes.c_size_t, _P, _P]
+        L.mp_mlp_bwd_fused.restype = _I
         L.mp_vocab_ce_workspace_bytes.argtypes = [_I, _I, _I]
         L.mp_vocab_ce_workspace_bytes.restype = ctypes.c_size_t
         L.mp_vocab_ce.argtypes = [_P, _P, _P, _P, _P, ctypes.c_size_t, _I, _I, _I, _I, _I, _P, _P]
@@ -194,6 +203,46 @@ def mp_mlp_bwd_shards(X, A, B, U, Y, dZ, dX, dA, dB, dU_ws, *, t: int, shard_beg
         _ptr(dU_ws, "dU_ws", shape=(T, f)), T, h, f, int(t), int(shard_begin), int(shard_count),
         _status_ptr(d_status), _stream(stream))
     _check("mp_mlp_bwd_shards", code)
+
+
+def mp_mlp_fused_workspace_bytes(T: int, h: int, f: int, t: int) -> int:
+    return int(lib().mp_mlp_fused_workspace_bytes(int(T), int(h), int(f), int(t)))
+
+
+def mp_mlp_fused_workspace(T: int, h: int, f: int, t: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for mp_mlp_fwd_fused / mp_mlp_bwd_fused (every call leaves it zero)."""
+    return torch.zeros(mp_mlp_fused_workspace_bytes(T, h, f, t), dtype=torch.uint8, device=device)
+
+
+def mp_mlp_fwd_fused(X, A, B, Z, Y, U_save=None, *, t: int, workspace, shard_begin: int = 0,
+                     shard_count: int | None = None, d_status=None, stream=None) -> None:
+    """mp_mlp_fwd_shards in one launch (both GEMMs of the forward); equal outputs bit for bit."""
+    T, h = X.shape
+    f = A.shape[1]
+    n = int(t) - int(shard_begin) if shard_count is None else int(shard_count)
+    wp, wb = _ws(workspace)
+    code = lib().mp_mlp_fwd_fused(
+        _ptr(X, "X", shape=(T, h)), _ptr(A, "A", shape=(h, f)), _ptr(B, "B", shape=(f, h)),
+        _ptr(Z, "Z", shape=(T, h)), _ptr(Y, "Y", shape=(T, f)),
+        _ptr(U_save, "U_save", shape=(T, f), allow_none=True),
+        T, h, f, int(t), int(shard_begin), n, wp, wb, _status_ptr(d_status), _stream(stream))
+    _check("mp_mlp_fwd_fused", code)
+
+
+def mp_mlp_bwd_fused(X, A, B, U, Y, dZ, dX, dA, dB, dU_ws, *, t: int, workspace, shard_begin: int = 0,
+                     shard_count: int | None = None, d_status=None, stream=None) -> None:
+    """mp_mlp_bwd_shards in one launch (dU, dX, dA, dB); equal outputs bit for bit."""
+    T, h = X.shape
+    f = A.shape[1]
+    n = int(t) - int(shard_begin) if shard_count is None else int(shard_count)
+    wp, wb = _ws(workspace)
+    code = lib().mp_mlp_bwd_fused(
+        _ptr(X, "X", shape=(T, h)), _ptr(A, "A", shape=(h, f)), _ptr(B, "B", shape=(f, h)),
+        _ptr(U, "U", shape=(T, f)), _ptr(Y, "Y", shape=(T, f)), _ptr(dZ, "dZ", shape=(T, h)),
+        _ptr(dX, "dX", shape=(T, h)), _ptr(dA, "dA", shape=(h, f)), _ptr(dB, "dB", shape=(f, h)),
+        _ptr(dU_ws, "dU_ws", shape=(T, f)), T, h, f, int(t), int(shard_begin), n, wp, wb,
+        _status_ptr(d_status), _stream(stream))
+    _check("mp_mlp_bwd_fused", code)
 
 
 def mp_vocab_ce_workspace_bytes(T: int, v_pad: int, t: int) -> int:

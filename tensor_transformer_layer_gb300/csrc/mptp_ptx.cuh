@@ -180,6 +180,25 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 }
 
 // ----------------------------------------------------------------------------
+// Completion counters in global memory between CTAs of one grid, for data that
+// TMA writes and TMA reads. The writer waits for its bulk stores to complete,
+// fences the async proxy against the generic one and publishes with a release
+// add; the reader polls with acquire loads and fences the other way before
+// issuing TMA loads.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// ----------------------------------------------------------------------------
 // tcgen05: tensor memory (TMEM) allocation, MMA, commit, loads.
 // ----------------------------------------------------------------------------
 // Whole warp; writes the allocated TMEM base address to *dst (shared memory).

@@ -114,6 +114,36 @@ def test_mlp_rejects_null_and_misaligned(L):
     assert L.mp_mlp_bwd(FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, 64, 128, 1, None, None) == 1
 
 
+def test_mlp_fused_workspace_bytes(L):
+    import tensor_transformer_layer_gb300 as mp
+    # 64 control words, then one counter per 256-row block and per 256-column tile of Y (dU),
+    # rounded up to 256 bytes.
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert mp.mp_mlp_fused_workspace_bytes(4096, 3072, 12288, 8) == a256(4 * (64 + 16 + 48))
+    assert mp.mp_mlp_fused_workspace_bytes(300, 256, 1024, 4) == a256(4 * (64 + 2 + 4))
+    assert mp.mp_mlp_fused_workspace_bytes(8, 96, 128, 1) == 0     # h % 64
+    assert mp.mp_mlp_fused_workspace_bytes(8, 64, 192, 2) == 0     # (f/t) % 64
+
+
+def test_mlp_fused_rejects_before_any_launch(L):
+    ws = 1 << 20
+    for T, h, f, t, code in ((-1, 64, 128, 1, 1), (8, 96, 128, 1, 2), (8, 64, 192, 2, 2)):
+        assert L.mp_mlp_fwd_fused(FAKE, FAKE, FAKE, FAKE, FAKE, None, T, h, f, t, 0, t, FAKE, ws, None, None) == code
+        assert L.mp_mlp_bwd_fused(*([FAKE] * 10), T, h, f, t, 0, t, FAKE, ws, None, None) == code
+    # shard range outside [0, t)
+    assert L.mp_mlp_fwd_fused(FAKE, FAKE, FAKE, FAKE, FAKE, None, 8, 64, 128, 2, 1, 2, FAKE, ws, None, None) == 1
+    assert L.mp_mlp_bwd_fused(*([FAKE] * 10), 8, 64, 128, 2, 2, 1, FAKE, ws, None, None) == 1
+    # workspace: NULL, misaligned or smaller than mp_mlp_fused_workspace_bytes -> MP_ERR_WORKSPACE
+    need = L.mp_mlp_fused_workspace_bytes(300, 256, 1024, 4)
+    bad = ctypes.c_void_p(0x100004)
+    for wp, wb in ((None, need), (bad, need), (FAKE, need - 4)):
+        assert L.mp_mlp_fwd_fused(FAKE, FAKE, FAKE, FAKE, FAKE, None, 300, 256, 1024, 4, 0, 4, wp, wb, None,
+                                  None) == 8
+        assert L.mp_mlp_bwd_fused(*([FAKE] * 10), 300, 256, 1024, 4, 0, 4, wp, wb, None, None) == 8
+    # T = 0 needs no workspace
+    assert L.mp_mlp_fwd_fused(None, None, None, None, None, None, 0, 64, 128, 2, 0, 2, None, 0, None, None) == 0
+
+
 def test_empty_batch_is_noop(L):
     assert L.mp_mlp_fwd(None, None, None, None, None, None, 0, 64, 128, 2, None, None) == 0
     assert L.mp_vocab_ce(None, None, None, None, None, 0, 0, 64, 256, 200, 2, None, None) == 0
@@ -141,6 +171,9 @@ def test_ce_rejects_small_workspace_and_misaligned(L):
 def test_no_device_answer(L):
     # Valid arguments on a machine without a GB300: MP_ERR_NO_DEVICE, nothing launched.
     assert L.mp_mlp_fwd(FAKE, FAKE, FAKE, FAKE, FAKE, None, 8, 64, 128, 1, None, None) == 4
+    assert L.mp_mlp_fwd_fused(FAKE, FAKE, FAKE, FAKE, FAKE, None, 8, 64, 128, 1, 0, 1, FAKE, 1 << 20, None,
+                              None) == 4
+    assert L.mp_mlp_bwd_fused(*([FAKE] * 10), 8, 64, 128, 1, 0, 1, FAKE, 1 << 20, None, None) == 4
     assert L.mp_vocab_ce(FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 30, 4, 64, 256, 200, 1, None, None) == 4
     # The no-allocation entry point: a T = 0 call also reaches the device (it places the static
     # array there), so without one it answers MP_ERR_NO_DEVICE; a problem whose triples fit the
