@@ -2,9 +2,9 @@
 
 One step = one pass of the whole path over one batch of synthetic input:
   * the sharded MLP block at the 8.3B-layer shape (T = 4096 tokens, h = 3072,
-    f = 12288, t = 8 shards): mp_mlp_fwd (column-parallel GEMM + GeLU, row-
-    parallel GEMM with the shard sum) then mp_mlp_bwd (dU with GeLU', dX with
-    the shard sum, dA, dB);
+    f = 12288, t = 8 shards): mp_mlp_fwd_fused (column-parallel GEMM + GeLU and
+    row-parallel GEMM with the shard sum, one launch) then mp_mlp_bwd_fused (dU
+    with GeLU', dX with the shard sum, dA, dB, one launch);
   * the vocab-parallel fused output GEMM + cross-entropy at the 1.2B-model
     shape (T = 8192, h = 1536, vocabulary 50,257 padded to 51,200, t = 8):
     mp_vocab_ce_partials then mp_vocab_ce_combine.
@@ -53,7 +53,7 @@ CE_8P3B = dict(T=4096, h=3072, v_pad=51200, v_valid=50257, t=8, seed=1006)
 SUSTAINED_S = 4.0     # seconds of back-to-back steps in the sustained leg
 SUSTAINED_CHUNK = 50  # steps between the sustained leg's CUDA events
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS_PER_STEP = 8  # fwd: 2, bwd: 4, CE: 2
+KERNELS_PER_STEP = 4  # MLP fwd: 1, MLP bwd: 1, CE: 2
 KERNEL_SOURCES = ("mptp_gemm.cuh", "mptp_ptx.cuh", "mptp_launch.cuh", "mptp_ce.cu")
 
 
@@ -270,6 +270,7 @@ class Step:
         self.d.update(Z=e(T, h), Y=e(T, f), U=e(T, f), dX=e(T, h), dA=e(h, f), dB=e(f, h), dU=e(T, f),
                       loss=e(c["T"], dt=torch.float32))
         self.ws = e(mp.mp_vocab_ce_workspace_bytes(c["T"], c["v_pad"], c["t"]), dt=torch.uint8)
+        self.mlp_ws = mp.mp_mlp_fused_workspace(T, h, f, m["t"], device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.out_names = ("Z", "dX", "dA", "dB", "loss")
 
@@ -283,8 +284,9 @@ class Step:
         mp, d = self.mp, self.d
         t = MLP["t"]
         kw = dict(d_status=self.status, stream=stream)
-        mp.mp_mlp_fwd(d["X"], d["A"], d["B"], d["Z"], d["Y"], d["U"], t=t, **kw)
-        mp.mp_mlp_bwd(d["X"], d["A"], d["B"], d["U"], d["Y"], d["dZ"], d["dX"], d["dA"], d["dB"], d["dU"], t=t, **kw)
+        mp.mp_mlp_fwd_fused(d["X"], d["A"], d["B"], d["Z"], d["Y"], d["U"], t=t, workspace=self.mlp_ws, **kw)
+        mp.mp_mlp_bwd_fused(d["X"], d["A"], d["B"], d["U"], d["Y"], d["dZ"], d["dX"], d["dA"], d["dB"], d["dU"], t=t,
+                            workspace=self.mlp_ws, **kw)
         if ev is not None:
             ev["ce0"].record()
         mp.mp_vocab_ce_partials(d["Xc"], d["E"], d["target"], self.ws, v_valid=CE["v_valid"], t=CE["t"], **kw)
@@ -338,13 +340,18 @@ def event_median(fn, reps, flush):
 
 
 def time_breakdown(step, reps, flush):
-    """Per-call device times (ms, median) of the step's four C-ABI calls."""
+    """Per-call device times (ms, median) of the step's four C-ABI calls, and of the MLP through the
+    separate-launch entry points (mp_mlp_fwd / mp_mlp_bwd: the same outputs, bit for bit) for
+    comparison."""
     import torch
-    mp, d, t = step.mp, step.d, MLP["t"]
+    mp, d, t, ws = step.mp, step.d, MLP["t"], step.mlp_ws
     calls = {
-        "mlp_fwd": lambda: mp.mp_mlp_fwd(d["X"], d["A"], d["B"], d["Z"], d["Y"], d["U"], t=t),
-        "mlp_bwd": lambda: mp.mp_mlp_bwd(d["X"], d["A"], d["B"], d["U"], d["Y"], d["dZ"], d["dX"], d["dA"],
-                                         d["dB"], d["dU"], t=t),
+        "mlp_fwd": lambda: mp.mp_mlp_fwd_fused(d["X"], d["A"], d["B"], d["Z"], d["Y"], d["U"], t=t, workspace=ws),
+        "mlp_bwd": lambda: mp.mp_mlp_bwd_fused(d["X"], d["A"], d["B"], d["U"], d["Y"], d["dZ"], d["dX"], d["dA"],
+                                               d["dB"], d["dU"], t=t, workspace=ws),
+        "mlp_fwd_separate": lambda: mp.mp_mlp_fwd(d["X"], d["A"], d["B"], d["Z"], d["Y"], d["U"], t=t),
+        "mlp_bwd_separate": lambda: mp.mp_mlp_bwd(d["X"], d["A"], d["B"], d["U"], d["Y"], d["dZ"], d["dX"], d["dA"],
+                                                  d["dB"], d["dU"], t=t),
         "ce_partials": lambda: mp.mp_vocab_ce_partials(d["Xc"], d["E"], d["target"], step.ws,
                                                        v_valid=CE["v_valid"], t=CE["t"]),
         "ce_combine": lambda: mp.mp_vocab_ce_combine(step.ws, d["target"], d["loss"], v_pad=CE["v_pad"],
@@ -798,7 +805,7 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true",
                     help="time MLP fwd+bwd and the fused CE at every point of the layer sweep (one JSON line each)")
     ap.add_argument("--profile-case", choices=("none", "ce", "ce_full", "ce_8p3b", "ce_bwd", "mlp", "mlp_small",
-                                               "mlp_split", "attn"),
+                                               "mlp_split", "mlp_chain", "mlp_chain_small", "attn"),
                     default="none",
                     help="run only a small case of one entry point a few times (for ncu), print nothing")
     args = ap.parse_args(argv)
@@ -936,7 +943,8 @@ def main(argv=None):
 def run_sweep(dev, reps, warmup):
     """MLP fwd+bwd and fused CE throughput at every sweep point: h in {1536, 1920, 2304,
     3072} (f = 4h), T in {2048, 8192}, t in {1, 2, 4, 8}, vocabulary 51,200 (50,257
-    valid). Median of `reps` launches, L2 flushed before each."""
+    valid). Median of `reps` launches, L2 flushed before each. The MLP runs through the
+    one-launch entry points; the separate-launch ones are timed beside them."""
     import torch
 
     import synth
@@ -959,21 +967,26 @@ def run_sweep(dev, reps, warmup):
             ci = synth.ce_inputs(T, h, 51200, 50257, seed=1004)
             Xc, E, tg = ci["X"].to(dev), ci["E"].to(dev), ci["target"].to(dev)
             loss = torch.empty(T, dtype=torch.float32, device=dev)
+            mws = mp.mp_mlp_fused_workspace(T, h, f, 8, device=dev)
             for t in (1, 2, 4, 8):
-                ms = med(lambda: (mp.mp_mlp_fwd(d["X"], d["A"], d["B"], Z, Y, U, t=t),
-                                  mp.mp_mlp_bwd(d["X"], d["A"], d["B"], U, Y, d["dZ"], dX, dA, dB, dU, t=t)))
+                ms = med(lambda: (mp.mp_mlp_fwd_fused(d["X"], d["A"], d["B"], Z, Y, U, t=t, workspace=mws),
+                                  mp.mp_mlp_bwd_fused(d["X"], d["A"], d["B"], U, Y, d["dZ"], dX, dA, dB, dU, t=t,
+                                                      workspace=mws)))
+                sep_ms = med(lambda: (mp.mp_mlp_fwd(d["X"], d["A"], d["B"], Z, Y, U, t=t),
+                                      mp.mp_mlp_bwd(d["X"], d["A"], d["B"], U, Y, d["dZ"], dX, dA, dB, dU, t=t)))
                 ws = torch.empty(mp.mp_vocab_ce_workspace_bytes(T, 51200, t), dtype=torch.uint8, device=dev)
                 ce_ms = med(lambda: mp.mp_vocab_ce(Xc, E, tg, loss, ws, v_valid=50257, t=t))
                 mlp_tf = 12.0 * T * h * f / (ms * 1e-3) / 1e12
                 ce_tf = 2.0 * T * h * 51200 / (ce_ms * 1e-3) / 1e12
                 print(json.dumps({
                     "sweep": True, "h": h, "f": f, "T": T, "t": t, "heads": h // 96,
-                    "mlp_fwd_bwd_ms": ms, "mlp_tflops": mlp_tf,
+                    "mlp_fwd_bwd_ms": ms, "mlp_tflops": mlp_tf, "mlp_separate_ms": sep_ms,
+                    "mlp_separate_tflops": 12.0 * T * h * f / (sep_ms * 1e-3) / 1e12,
                     "ce_ms": ce_ms, "ce_tflops": ce_tf, "ce_tokens_per_s": T / (ce_ms * 1e-3),
                     "pct_of_measured_bf16_sustained": {"mlp": mlp_tf / peaks["bf16_tflops_sustained"],
                                                        "ce": ce_tf / peaks["bf16_tflops_sustained"]},
                     "peak_source": peak_src}), flush=True)
-            del d, Z, Y, U, dX, dA, dB, dU, Xc, E, tg
+            del d, Z, Y, U, dX, dA, dB, dU, Xc, E, tg, mws
             torch.cuda.empty_cache()
     return 0
 
@@ -982,7 +995,9 @@ def profile_case(which, dev):
     """Cases for ncu captures: 'ce' (T=2048), 'ce_8p3b' (T=4096, h=3072: 0.35 GB) and 'mlp' (the 8.3B
     layer, 0.7 GB) are small enough for multi-pass captures (under 1 GB on the device, 0.2-0.7 ms
     kernels, inputs > L2); 'mlp_small' is the sweep's T = 2048, h = 1536 point and 'mlp_split' its
-    T = 2048, h = 3072 point (K2 on the split-K kernel); 'ce_full' is the bench's CE launch, for
+    T = 2048, h = 3072 point (K2 on the split-K kernel); 'mlp_chain' and 'mlp_chain_small' run the
+    one-launch forward and backward at the 8.3B layer and at T = 2048, h = 1536 (the other 'mlp'
+    cases run the separate-launch kernels); 'ce_full' is the bench's CE launch, for
     one-pass metrics only; 'ce_bwd' is the CE backward on the bench's CE workload from the exported
     log-sum-exp, one call shard by shard and then one call in one pass (1.3 GB on the device; for
     the one-pass launch list)."""
@@ -1035,13 +1050,20 @@ def profile_case(which, dev):
             T, h, f = 2048, 1536, 6144
         if which == "mlp_split":   # T = 2048, h = 3072: the row-parallel GEMM split over two pairs
             T, h, f = 2048, 3072, 12288
+        if which == "mlp_chain_small":   # the one-launch forward and backward at T = 2048, h = 1536
+            T, h, f = 2048, 1536, 6144
         mi = synth.mlp_inputs(T, h, f, seed=MLP["seed"])
         d = {k: v.to(dev) for k, v in mi.items()}
         e = lambda *s: torch.empty(*s, dtype=torch.bfloat16, device=dev)
         Z, Y, U, dX, dA, dB, dU = e(T, h), e(T, f), e(T, f), e(T, h), e(h, f), e(f, h), e(T, f)
+        ws = mp.mp_mlp_fused_workspace(T, h, f, t, device=dev)
         for _ in range(3):
-            mp.mp_mlp_fwd(d["X"], d["A"], d["B"], Z, Y, U, t=t)
-            mp.mp_mlp_bwd(d["X"], d["A"], d["B"], U, Y, d["dZ"], dX, dA, dB, dU, t=t)
+            if which.startswith("mlp_chain"):
+                mp.mp_mlp_fwd_fused(d["X"], d["A"], d["B"], Z, Y, U, t=t, workspace=ws)
+                mp.mp_mlp_bwd_fused(d["X"], d["A"], d["B"], U, Y, d["dZ"], dX, dA, dB, dU, t=t, workspace=ws)
+            else:
+                mp.mp_mlp_fwd(d["X"], d["A"], d["B"], Z, Y, U, t=t)
+                mp.mp_mlp_bwd(d["X"], d["A"], d["B"], U, Y, d["dZ"], dX, dA, dB, dU, t=t)
     torch.cuda.synchronize()
     return 0
 
