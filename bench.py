@@ -54,7 +54,11 @@ SUSTAINED_S = 4.0     # seconds of back-to-back steps in the sustained leg
 SUSTAINED_CHUNK = 50  # steps between the sustained leg's CUDA events
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNELS_PER_STEP = 4  # MLP fwd: 1, MLP bwd: 1, CE: 2
-KERNEL_SOURCES = ("mptp_gemm.cuh", "mptp_ptx.cuh", "mptp_launch.cuh", "mptp_ce.cu")
+# Sources whose hash a committed ncu summary records, per kernel: its DRAM counters are reported only
+# while they still describe the code that runs.
+CE_SOURCES = ("mptp_gemm.cuh", "mptp_ptx.cuh", "mptp_launch.cuh", "mptp_ce.cu")
+CHAIN_SOURCES = ("mptp_gemm_chain.cuh", "mptp_gemm.cuh", "mptp_gemm_split.cuh", "mptp_ptx.cuh", "mptp_launch.cuh",
+                 "mptp_mlp_fused.cu")
 
 
 def mlp_flop(w=MLP):
@@ -102,12 +106,12 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(sources=CE_SOURCES):
     """sha256[:16] of the kernel sources with comments and blank lines removed, so that a
     recorded profile stays valid across comment-only edits."""
     import re
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources:
         with open(os.path.join(ROOT, "tensor_transformer_layer_gb300", "csrc", name)) as fh:
             text = fh.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
@@ -117,7 +121,7 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name="ce_logits_lse_ncu.txt"):
+def profiled_traffic(name="ce_logits_lse_ncu.txt", sources=CE_SOURCES):
     """DRAM bytes per launch of a kernel from its committed ncu summary, or None when
     the kernel sources changed since those counters were taken."""
     path = os.path.join(ROOT, "profiles", name)
@@ -127,7 +131,7 @@ def profiled_traffic(name="ce_logits_lse_ncu.txt"):
     except OSError:
         return None
     kv = {k.strip(): v.strip() for k, v in kv.items()}
-    if kv.get("kernel_source_hash") != kernel_source_hash():
+    if kv.get("kernel_source_hash") != kernel_source_hash(sources):
         return None
     try:
         return float(kv["dram_bytes_per_full_launch"])
@@ -280,13 +284,17 @@ class Step:
 
     def run(self, ev=None, stream=None):
         """One step on `stream` (default: the current stream). ev: optional dict of CUDA
-        events to record around the CE logit kernel."""
+        events to record around the MLP backward launch (b0, b1) and the CE logit kernel (ce0, ce1)."""
         mp, d = self.mp, self.d
         t = MLP["t"]
         kw = dict(d_status=self.status, stream=stream)
         mp.mp_mlp_fwd_fused(d["X"], d["A"], d["B"], d["Z"], d["Y"], d["U"], t=t, workspace=self.mlp_ws, **kw)
+        if ev is not None:
+            ev["b0"].record()
         mp.mp_mlp_bwd_fused(d["X"], d["A"], d["B"], d["U"], d["Y"], d["dZ"], d["dX"], d["dA"], d["dB"], d["dU"], t=t,
                             workspace=self.mlp_ws, **kw)
+        if ev is not None:
+            ev["b1"].record()
         if ev is not None:
             ev["ce0"].record()
         mp.mp_vocab_ce_partials(d["Xc"], d["E"], d["target"], self.ws, v_valid=CE["v_valid"], t=CE["t"], **kw)
@@ -309,7 +317,7 @@ def time_device(step, steps, warmup, flush):
     torch.cuda.synchronize()
     evs = []
     for _ in range(steps):
-        ev = {k: torch.cuda.Event(enable_timing=True) for k in ("s0", "s1", "ce0", "ce1")}
+        ev = {k: torch.cuda.Event(enable_timing=True) for k in ("s0", "s1", "b0", "b1", "ce0", "ce1")}
         ev["s0"].record()
         step.run(ev)
         ev["s1"].record()
@@ -318,7 +326,8 @@ def time_device(step, steps, warmup, flush):
     torch.cuda.synchronize()
     step_ms = [e["s0"].elapsed_time(e["s1"]) for e in evs]
     ce_ms = [e["ce0"].elapsed_time(e["ce1"]) for e in evs]
-    return step_ms, ce_ms
+    bwd_ms = [e["b0"].elapsed_time(e["b1"]) for e in evs]
+    return step_ms, ce_ms, bwd_ms
 
 
 def event_median(fn, reps, flush):
@@ -851,7 +860,7 @@ def main(argv=None):
     torch.cuda.synchronize()
     sampler = ClockSampler(physical_gpu(local_rank))
     sampler.start()
-    step_ms, ce_ms = time_device(step, args.steps, args.warmup, flush)
+    step_ms, ce_ms, bwd_ms = time_device(step, args.steps, args.warmup, flush)
     clocks = sampler.stop()
     torch.cuda.synchronize()
     barrier(world)
@@ -883,6 +892,9 @@ def main(argv=None):
     ce_avg_ms = sum(ce_ms) / len(ce_ms)
     ce_achieved = ce_flop() / (ce_avg_ms * 1e-3) / 1e12
     traffic = profiled_traffic()
+    bwd_avg_ms = sum(bwd_ms) / len(bwd_ms)
+    bwd_flop = 8.0 * MLP["T"] * MLP["h"] * MLP["f"]   # dU, dX, dA, dB: four 2 T h f products
+    bwd_achieved = bwd_flop / (bwd_avg_ms * 1e-3) / 1e12
     mlp_ms = breakdown["mlp_fwd"] + breakdown["mlp_bwd"]
     ce_call_ms = breakdown["ce_partials"] + breakdown["ce_combine"]
 
@@ -912,7 +924,16 @@ def main(argv=None):
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(),
             "gpu_launches": KERNELS_PER_STEP * (args.steps),
             "clocks": clocks,
-            "roofline": {"kernel": "K6 mp_vocab_ce_partials (logit GEMM + online LSE epilogue)", "bound": "tensor",
+            "roofline": {"kernel": "MLP backward in one launch (gemm_chain_kernel: K3 dU with GeLU', K4 dX with the "
+                                   "f sum, K5a dA, K5b dB), the step's longest kernel", "bound": "tensor",
+                         "achieved": bwd_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": bwd_achieved / peaks["bf16_tflops"],
+                         "peak_source": f"{peak_src} bf16 burst (timed inside short steps)",
+                         "traffic": profiled_traffic("mlp_chain_8p3b_ncu.txt", CHAIN_SOURCES),
+                         "algorithmic_flop_per_launch": bwd_flop, "avg_launch_ms": bwd_avg_ms,
+                         "theoretical_at_sampled_clock": theo_sampled,
+                         "frac_of_theoretical_at_sampled_clock": bwd_achieved / theo_sampled},
+            "roofline_ce": {"kernel": "K6 mp_vocab_ce_partials (logit GEMM + online LSE epilogue)", "bound": "tensor",
                          "achieved": ce_achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                          "frac": ce_achieved / peaks["bf16_tflops"],
                          "peak_source": f"{peak_src} bf16 burst (timed inside short steps)", "traffic": traffic,
