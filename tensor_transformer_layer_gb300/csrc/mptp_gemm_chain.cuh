@@ -59,7 +59,7 @@ constexpr int CHAIN_MAX_PROBS = 4;
 constexpr int CHAIN_MAX_SEGS = 64;
 constexpr int CHAIN_MAX_PAIRS = 96;      // CTA pairs a launch may have (GB300: 76)
 constexpr int CHAIN_MAX_SCHED = 4096;    // list positions a precomputed schedule may hold
-constexpr int CHAIN_MAX_PER_PAIR = 512;  // ... and one pair's share of them
+constexpr int CHAIN_MAX_PER_PAIR = 480;  // ... and one pair's share of them
 constexpr int CHAIN_CTL_WORDS = 64;  // word 1: finished CTAs; padding to 256 bytes
 constexpr int CHAIN_BN = 256;
 static_assert(CHAIN_BN == 4 * BK, "a dependency tile is four K blocks");
@@ -125,11 +125,9 @@ struct ChainCfg {
     static constexpr int STG_PER_WARP = STG_BYTES_PER_WARP;
     static constexpr int STG_BYTES = NE * STG_PER_WARP;
     // problem table, list segments, this pair's list positions, TMEM slot and flags words
-    static constexpr int EXTRA = 2048;
-    static_assert(CHAIN_MAX_PROBS * 40 + CHAIN_MAX_SEGS * 12 + CHAIN_MAX_PER_PAIR * 2 + 16 <= EXTRA,
-                  "chain bookkeeping in shared memory");
-    static constexpr int FIT_STAGES = static_cast<int>((SMEM_LIMIT - 1024 - 512 - EXTRA - STG_BYTES) / STAGE_BYTES);
-    static constexpr int STAGES = FIT_STAGES < 8 ? FIT_STAGES : 8;
+    static constexpr int EXTRA = CHAIN_MAX_PROBS * 40 + CHAIN_MAX_SEGS * 12 + CHAIN_MAX_PER_PAIR * 2 + 16;
+    // Six stages with either epilogue width (eight warps' staging boxes leave 8 bytes to spare).
+    static constexpr int STAGES = 6;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + STG_BYTES + 8 * NUM_BARS + EXTRA;
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory per block");
