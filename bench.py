@@ -57,8 +57,7 @@ KERNELS_PER_STEP = 4  # MLP fwd: 1, MLP bwd: 1, CE: 2
 # Sources whose hash a committed ncu summary records, per kernel: its DRAM counters are reported only
 # while they still describe the code that runs.
 CE_SOURCES = ("mptp_gemm.cuh", "mptp_ptx.cuh", "mptp_launch.cuh", "mptp_ce.cu")
-CHAIN_SOURCES = ("mptp_gemm_chain.cuh", "mptp_gemm.cuh", "mptp_gemm_split.cuh", "mptp_ptx.cuh", "mptp_launch.cuh",
-                 "mptp_mlp_fused.cu")
+CHAIN_SOURCES = ("mptp_gemm_chain.cuh", "mptp_gemm.cuh", "mptp_ptx.cuh", "mptp_launch.cuh", "mptp_mlp_fused.cu")
 
 
 def mlp_flop(w=MLP):

@@ -51,7 +51,7 @@
 
 #include <type_traits>
 
-#include "mptp_gemm_split.cuh"
+#include "mptp_gemm.cuh"
 
 namespace mptp {
 

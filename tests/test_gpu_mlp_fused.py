@@ -217,3 +217,24 @@ def test_fused_empty_batch():
                         torch.empty(0, h, dtype=torch.bfloat16, device="cuda"), dA, dB, e, t=t, workspace=ws)
     torch.cuda.synchronize()
     assert int(dA.count_nonzero().item()) == 0 and int(dB.count_nonzero().item()) == 0
+
+
+def test_fused_beyond_the_schedule_tables_round_robin():
+    # T = 32768, h = 2048, f = 8192: 5120 forward and 5632 backward units, more list positions than a
+    # precomputed schedule holds (4096), so each pair runs list positions p, p + P, ... instead.
+    # Bitwise against the separate launches (no split-K at this size), sampled rows against the oracle.
+    mp = _mp()
+    T, h, f, t = 32768, 2048, 8192, 4
+    inp = synth.mlp_inputs(T, h, f, seed=7700)
+    dev = run_mlp_fwd(inp, t)
+    ws = mp.mp_mlp_fused_workspace(T, h, f, t)
+    Z, Y, U = fused_fwd(mp, dev["X"], dev["A"], dev["B"], t, ws)
+    assert torch.equal(Z, dev["Z"]) and torch.equal(Y, dev["Y"]) and torch.equal(U, dev["U"])
+    del Y, U
+    sep = run_mlp_bwd(dev, inp["dZ"], t)
+    g = fused_bwd(mp, dev["X"], dev["A"], dev["B"], dev["U"], dev["Y"], inp["dZ"].cuda(), t, ws)
+    for k in ("dU", "dX", "dA", "dB"):
+        assert torch.equal(g[k], sep[k]), k
+    rows = synth.sample_indices(T, 8, seed=7701).numpy()
+    _, _, Zr = oracle.mlp_fwd_rows(f64(inp["X"]), f64(inp["A"]), f64(inp["B"]), rows)
+    assert rel_fro(f64(Z)[rows], Zr) <= Z_REL_FRO
