@@ -181,8 +181,14 @@ MP_API mp_status mp_mlp_bwd_shards(const mp_bf16* X, const mp_bf16* A, const mp_
  *     It holds a few control words and one completion counter per 256-token row
  *     block and per 256-column tile of Y (dU). Every call returns it to zeros when
  *     its kernel ends, also after a timeout, so consecutive calls on one stream may
- *     share it; calls that can run at the same time on the GPU (different streams)
- *     need a workspace each.
+ *     share it.
+ *   Concurrency: a call's kernel takes every SM (one CTA pair per two SMs) and
+ *     relies on all of its CTAs running at once, since a tile may wait for a tile of
+ *     another CTA pair. Run these calls alone on the device; kernels enqueued before
+ *     them on the same stream are fine. Beside another kernel on a different stream
+ *     (or another of these calls), a CTA pair can wait for one that is not resident;
+ *     the bounded wait then ends the call with MP_DEV_TIMEOUT instead of a hang.
+ *     The separate-launch entry points have no such requirement.
  *     Smaller, NULL or misaligned: MP_ERR_WORKSPACE, nothing launched.
  *   Size rules, shard range and outputs as mp_mlp_fwd_shards / mp_mlp_bwd_shards;
  *   dU_ws as mp_mlp_bwd. T = 0: nothing to compute (the backward zeroes its dA and

@@ -38,9 +38,11 @@
 // it is never blocked, provided its CTAs are resident. The grid is sized to the
 // pairs the device holds at once (one CTA per SM); CTAs that start before the
 // previous kernel in the stream has left the SMs wait only for that kernel, which
-// does not depend on them. Every wait is still bounded (MP_DEV_TIMEOUT, as in
-// mptp_gemm.cuh), so a pair kept off the device by other work ends the launch
-// with an error instead of a hang.
+// does not depend on them. A kernel running beside this one on another stream can
+// keep a pair off the device while the resident pairs wait for it; every wait is
+// bounded (MP_DEV_TIMEOUT, as in mptp_gemm.cuh), so that ends the launch with an
+// error instead of a hang, and the entry points document that these launches run
+// alone on the device.
 //
 // Workspace (caller-owned, zero before first use): word 1 counts the CTAs that have
 // finished; after the control words come the row-block counters and the column-tile
