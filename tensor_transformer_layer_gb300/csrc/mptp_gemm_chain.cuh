@@ -47,8 +47,7 @@
 // Workspace (caller-owned, zero before first use): word 1 counts the CTAs that have
 // finished; after the control words come the row-block counters and the column-tile
 // counters of the first GEMM (K1 or K3). The last CTA to finish zeroes all of it
-// again, so consecutive launches on one stream can share it; launches that may
-// overlap on the GPU need a workspace each.
+// again, so consecutive launches on one stream can share it.
 #pragma once
 
 #include <type_traits>
@@ -75,7 +74,7 @@ enum ChainDep : int {
 };
 
 struct ChainProb {
-    ProbInfo pr;   // M, N, row blocks, units, K range, operand majorness (pr.n_fastest unused)
+    ProbInfo pr;   // M, N, row blocks, units, K range, operand majorness (pr.n_fastest not used here)
     int ncols;     // column tiles a row block has
     int group;     // unit order: row blocks in groups of `group`, row blocks fastest within a group
     int dep;       // ChainDep on problem 0
