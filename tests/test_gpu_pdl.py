@@ -2,7 +2,7 @@
 its predecessor in the stream finishes and waits for it before touching global memory. The
 results must not depend on it (bitwise equal with MPTP_PDL=0), and a step captured into a
 CUDA graph (where the dependencies become programmatic edges) must replay to the eager
-result."""
+result, with the MLP as six launches or as one launch per direction."""
 import os
 
 import pytest
@@ -110,3 +110,41 @@ def test_pdl_attention_block_bitwise():
         res[mode] = (qkv, o, out)
     for a, c in zip(res["1"], res["0"]):
         assert torch.equal(a, c)
+
+
+def _fused_step(d, t, v_valid, st):
+    m = mp()
+    m.mp_mlp_fwd_fused(d["X"], d["A"], d["B"], d["Z"], d["Y"], d["U"], t=t, workspace=d["mws"], d_status=st)
+    m.mp_mlp_bwd_fused(d["X"], d["A"], d["B"], d["U"], d["Y"], d["dZ"], d["dX"], d["dA"], d["dB"], d["dU"], t=t,
+                       workspace=d["mws"], d_status=st)
+    m.mp_vocab_ce(d["Xc"], d["E"], d["target"], d["loss"], d["ws"], v_valid=v_valid, t=t, d_status=st)
+
+
+@pytest.mark.parametrize("T,h,f", [(640, 256, 1024), (2048, 1536, 6144)])
+def test_fused_step_in_cuda_graph(T, h, f):
+    # The bench's step (each MLP direction in one launch, then the fused loss) captured into a CUDA
+    # graph: the one-launch kernels' workspace is returned to zeros inside each launch, so every
+    # replay starts from a clean workspace and reproduces the eager step bit for bit.
+    shape = dict(SHAPE, T=T, h=h, f=f)
+    d = _buffers(**shape, seed=13300)
+    d["mws"] = mp().mp_mlp_fused_workspace(T, h, f, shape["t"])
+    st = status_tensor()
+    with _Env("MPTP_PDL", "1"):
+        _fused_step(d, shape["t"], shape["v_valid"], st)
+        torch.cuda.synchronize()
+        want = {k: d[k].clone() for k in OUTS}
+        for k in OUTS:
+            d[k].zero_()
+        torch.cuda.synchronize()
+        s = torch.cuda.Stream()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(graph, stream=s):
+                _fused_step(d, shape["t"], shape["v_valid"], st)
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert int(d["mws"].count_nonzero().item()) == 0
+    for k in OUTS:
+        assert torch.equal(d[k], want[k]), k
