@@ -7,10 +7,9 @@
 // section 3.4; "Tensor and pipeline parallelism, and choosing a layout",
 // Proposition (Megatron MLP split)), tile for tile with the same K-loops, so every
 // output equals theirs bit for bit. What changes is the schedule: the second GEMM
-// of the forward starts on a row block as soon as the first has produced the
-// columns it reads next, and in the backward the f sum (K4) and the weight
-// gradients (K5a, K5b) run beside K3 and each other on whichever CTA pairs are
-// free. That overlap is the method's own ("Tensor and pipeline parallelism, and
+// of the forward starts on a row block as soon as the first has completed that
+// row block, and in the backward the f sum (K4) and the weight gradients (K5a,
+// K5b) run beside K3 and each other on whichever CTA pairs are free. That overlap is the method's own ("Tensor and pipeline parallelism, and
 // choosing a layout", the remarks after the Proposition: the backward all-reduce
 // of dX overlaps the weight-gradient GEMMs), done inside one grid.
 #include <algorithm>
