@@ -168,28 +168,30 @@ MP_API mp_status mp_mlp_bwd_shards(const mp_bf16* X, const mp_bf16* A, const mp_
  * as mp_mlp_fwd_shards / mp_mlp_bwd_shards (same arguments, same outputs, equal
  * bit for bit), scheduled differently. In the forward, the row-parallel GEMM
  * (Z = sum_i Y_i B_i) starts on a block of 256 tokens as soon as the
- * column-parallel GEMM has written the columns of Y it reads next; in the
- * backward, dX (the f sum), dA and dB start as soon as the dU columns they read
- * exist, on whichever SMs are free. This is the overlap the method describes
- * between the backward all-reduce and the weight-gradient GEMMs ("Tensor and
- * pipeline parallelism, and choosing a layout", section 3, the remarks after the
- * Proposition), inside one grid, and it removes the part-empty last wave and the
- * ramp of every GEMM but the last.
+ * column-parallel GEMM has written that block's rows of Y. In the backward, dX
+ * (the f sum) starts on a block of tokens once its rows of dU exist, dA on a
+ * 256-column tile of dU once that tile exists, and dB at once, on whichever SMs
+ * are free. This is the overlap the method describes between the backward
+ * all-reduce and the weight-gradient GEMMs ("Tensor and pipeline parallelism, and
+ * choosing a layout", section 3, the remarks after the Proposition), inside one
+ * grid, and it removes the part-empty last wave and the ramp of every GEMM but
+ * the last.
  *
  *   workspace: mp_mlp_fused_workspace_bytes(T, h, f, t) bytes of device memory,
  *     16-byte aligned, ZERO-FILLED before its first use (e.g. cudaMemset once).
  *     It holds a few control words and one completion counter per 256-token row
  *     block and per 256-column tile of Y (dU). Every call returns it to zeros when
  *     its kernel ends, also after a timeout, so consecutive calls on one stream may
- *     share it.
+ *     share it (and a CUDA graph may replay a captured call). Smaller, NULL or
+ *     misaligned: MP_ERR_WORKSPACE, nothing launched.
  *   Concurrency: a call's kernel takes every SM (one CTA pair per two SMs) and
  *     relies on all of its CTAs running at once, since a tile may wait for a tile of
  *     another CTA pair. Run these calls alone on the device; kernels enqueued before
  *     them on the same stream are fine. Beside another kernel on a different stream
- *     (or another of these calls), a CTA pair can wait for one that is not resident;
- *     the bounded wait then ends the call with MP_DEV_TIMEOUT instead of a hang.
- *     The separate-launch entry points have no such requirement.
- *     Smaller, NULL or misaligned: MP_ERR_WORKSPACE, nothing launched.
+ *     (or another of these calls), or where the process may use fewer SMs than the
+ *     device has (an MPS limit on active threads), a CTA pair can wait for one that
+ *     is not resident; the bounded wait then ends the call with MP_DEV_TIMEOUT
+ *     instead of a hang. The separate-launch entry points have no such requirement.
  *   Size rules, shard range and outputs as mp_mlp_fwd_shards / mp_mlp_bwd_shards;
  *   dU_ws as mp_mlp_bwd. T = 0: nothing to compute (the backward zeroes its dA and
  *   dB range, as mp_mlp_bwd_shards does) and the workspace is not touched.
