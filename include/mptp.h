@@ -279,8 +279,15 @@ MP_API mp_status mp_vocab_ce_lse(const mp_bf16* X, const mp_bf16* E, const int32
  *   mp_vocab_ce on the same X, E, target), dloss [T] fp32 (upstream gradient, e.g.
  *   1/T for a mean) -> dX [T, h] bf16, dE [v_pad, h] bf16 (overwritten).
  *   workspace >= mp_vocab_ce_bwd_workspace_bytes(T, h, v_pad, t) bytes: the
- *   log-sum-exp [T], an fp32 dX accumulator [T, h] and one shard of dZ [T, v_pad/t];
- *   the shards are processed one after another (three GEMMs each).
+ *   log-sum-exp [T], a few hundred bytes of counters (the call zeroes them), an fp32
+ *   dX accumulator [T, h] and one shard of dZ [T, v_pad/t]; no initial value needed.
+ *   The shards are processed one after another, each shard's three GEMMs in ONE
+ *   kernel launch (dX and dE tiles start as soon as the dZ rows or columns they read
+ *   exist). That launch takes every SM and relies on all of its CTAs running at once,
+ *   so the same concurrency rule as mp_mlp_fwd_fused applies: run it alone on the
+ *   device (beside other kernels it ends with MP_DEV_TIMEOUT rather than hang).
+ *   MPTP_CE_BWD_CHAIN=0 in the environment runs each shard as three separate
+ *   launches instead, with no such rule; the gradients are the same bit for bit.
  *   workspace >= mp_vocab_ce_bwd_workspace_bytes_one_pass(T, h, v_pad, t) bytes
  *   (the log-sum-exp and every shard's dZ, [T, v_pad] bf16: 839 MB at T = 8192,
  *   v_pad = 51,200): dZ of all shards is formed in one launch, then dE and dX in

@@ -13,10 +13,19 @@
 //        forward's all-reduce would carry: shard 0's tiles are stored, later shards' tiles
 //        added at L2 by TMA reductions, and the last shard adds the accumulator in registers
 //        and stores bf16).
+// Shard by shard, each shard's three GEMMs run as one launch of the chain kernel
+// (mptp_gemm_chain.cuh): a K12 tile starts on a block of tokens once K10 has written
+// that block's dZ rows, a K11 tile once K10 has written its 256 vocabulary columns,
+// so the GEMMs share the SMs instead of each ending in a part-empty wave. The tiles
+// and K-loops are the separate kernels' (MPTP_CE_BWD_CHAIN=0 runs those instead), so
+// the gradients are the same bit for bit. With every shard's dZ in the workspace (one
+// pass), the three GEMMs run once each over the whole vocabulary.
 // The log-sum-exp comes from the forward: either exported by it (mp_vocab_ce_lse, then
 // mp_vocab_ce_bwd_lse), or rebuilt from its loss: lse = loss + z_target, with z_target
 // = X[r] . E[target[r]] recomputed in fp32 (K9, mp_vocab_ce_bwd).
-#include "mptp_gemm.cuh"
+#include <cstdlib>
+
+#include "mptp_gemm_chain.cuh"
 #include "mptp_internal.h"
 
 namespace mptp {
@@ -58,10 +67,11 @@ __global__ void __launch_bounds__(256) ce_lse_kernel(const __nv_bfloat16* __rest
     if (lane == 0) lse[r] = loss[r] + acc;
 }
 
-// Workspace: lse [T] fp32, then either (shard by shard, t > 1) an fp32 dX accumulator [T, h] and
-// one shard's dZ [T, v_pad / t] bf16, or (one pass, `chunks` = 1) every shard's dZ [T, v_pad] bf16.
+// Workspace: lse [T] fp32, then either (shard by shard, t > 1) the chain kernel's counters, an fp32
+// dX accumulator [T, h] and one shard's dZ [T, v_pad / t] bf16, or (one pass, `chunks` = 1) every
+// shard's dZ [T, v_pad] bf16.
 struct CeBwdLayout {
-    size_t lse_off, acc_off, dz_off, total;
+    size_t lse_off, ctr_off, ctr_bytes, acc_off, dz_off, total;
     int chunks;  // vocabulary chunks processed one after another: t (shard by shard) or 1
 };
 
@@ -72,7 +82,9 @@ static bool ce_bwd_layout(int T, int h, int v_pad, int t, bool one_pass, CeBwdLa
     L->chunks = one_pass ? 1 : t;
     const size_t vc = static_cast<size_t>(v_pad / L->chunks);
     L->lse_off = 0;
-    L->acc_off = align256(size_t(T) * 4);
+    L->ctr_off = align256(size_t(T) * 4);
+    L->ctr_bytes = L->chunks == 1 ? 0 : chain_counter_bytes(T, static_cast<int>(vc));  // one chunk: no chain
+    L->acc_off = L->ctr_off + L->ctr_bytes;
     L->dz_off = L->acc_off + (L->chunks == 1 ? 0 : align256(size_t(T) * h * 4));  // one chunk: no accumulator
     L->total = L->dz_off + align256(size_t(T) * vc * 2);
     return true;
@@ -142,6 +154,51 @@ static mp_status ce_bwd(const mp_bf16* X, const mp_bf16* E, const int32_t* targe
     const int vs = v_pad / C;
     const double Tb = 2.0 * T, hb = 2.0 * h, vb = 2.0 * vs;
     const unsigned long long budget = wait_budget_ns();
+    const char* chain_env = std::getenv("MPTP_CE_BWD_CHAIN");
+    if (C > 1 && !(chain_env && chain_env[0] == '0' && chain_env[1] == '\0')) {
+        // Each shard's K10, K12 and K11 in one chain launch; its counters start at zero and every
+        // launch returns them to zero for the next.
+        uint32_t* ctr = reinterpret_cast<uint32_t*>(ws + lay.ctr_off);
+        if (cudaMemsetAsync(ctr, 0, lay.ctr_bytes, s) != cudaSuccess) return MP_ERR_CUDA;
+        for (int i = 0; i < C; ++i) {
+            const __nv_bfloat16* Ei = Eb + static_cast<long long>(i) * vs * h;
+            __nv_bfloat16* dEi = reinterpret_cast<__nv_bfloat16*>(dE) + static_cast<long long>(i) * vs * h;
+            ChainMaps m{};
+            ChainArgs a{};
+            // problem 0, K10: z_i = X E_i^T -> dZ_i (both operands K-major)
+            if (!make_tmap_bf16(&m.m[0].a, X, h, T, h, 64, BM) ||
+                !make_tmap_bf16(&m.m[0].b, Ei, h, vs, h, 64, CHAIN_BN / 2) ||
+                !make_tmap_bf16_out(&m.m[0].o0, dz, vs, T, vs))
+                return MP_ERR_CUDA;
+            a.p[0] = chain_problem(T, vs, 0, h / BK, 0, 0, 1);
+            // problem 1, K12: dX (+)= dZ_i E_i (E_i MN-major), reads K10's rows
+            int b12 = 0;
+            if (!make_tmap_bf16(&m.m[1].a, dz, vs, T, vs, 64, BM) || !(b12 = make_tmap_mn_operand(&m.m[1].b, Ei, h, vs, h)) ||
+                !make_tmap_bf16_out(&m.m[1].o0, dX, h, T, h) || !make_tmap_f32_out(&m.m[1].o1, acc, h, T, h))
+                return MP_ERR_CUDA;
+            a.p[1] = chain_problem(T, h, 0, vs / BK, 0, b12, 1);
+            a.p[1].dep = DEP_ROWS;
+            // problem 2, K11: dE_i = dZ_i^T X (both MN-major), tile i of its rows reads K10's column tile i
+            int a11 = 0, b11 = 0;
+            if (!(a11 = make_tmap_mn_operand(&m.m[2].a, dz, vs, T, vs)) || !(b11 = make_tmap_mn_operand(&m.m[2].b, X, h, T, h)) ||
+                !make_tmap_bf16_out(&m.m[2].o0, dEi, h, vs, h))
+                return MP_ERR_CUDA;
+            a.p[2] = chain_problem(vs, h, 0, ceil_div(T, BK), a11, b11, ceil_div(vs, 2 * BM));
+            a.p[2].dep = DEP_COLS_M;
+            a.target = target;
+            a.lse = lse;
+            a.dloss = dloss;
+            a.v_valid = v_valid;
+            a.col_off = i * vs;
+            a.acc = acc;
+            a.ld_acc = h;
+            a.acc_mode = i == 0 ? ACC_FIRST : (i == C - 1 ? ACC_LAST : ACC_MID);
+            a.status = d_status;
+            a.budget_ns = budget;
+            if ((st = launch_chain_ce(m, a, sms, s, ctr)) != MP_OK) return st;
+        }
+        return MP_OK;
+    }
     for (int i = 0; i < C; ++i) {
         const __nv_bfloat16* Ei = Eb + static_cast<long long>(i) * vs * h;
         __nv_bfloat16* dEi = reinterpret_cast<__nv_bfloat16*>(dE) + static_cast<long long>(i) * vs * h;

@@ -1,6 +1,7 @@
 // A chain of dependent GEMMs in one persistent launch: the MLP block's forward
-// (K1 then K2) or backward (K3, then K4, K5a, K5b) with no kernel boundary
-// between them.
+// (K1 then K2) or backward (K3, then K4, K5a, K5b), or one vocabulary shard of the
+// cross-entropy backward (K10, then K12 and K11), with no kernel boundary between
+// them.
 //
 // Why. Each separate GEMM launch ends in a part-empty last round of tiles, an
 // epilogue with nothing to hide behind and a teardown, and the next launch
@@ -15,6 +16,8 @@
 //   K4 unit (m, n)                         needs K3's row block m
 //   K5a unit (h block i, f tile j)         needs K3's column tile j
 //   K5b                                    needs nothing (Y and dZ are inputs)
+//   K12 unit (m, n)                        needs K10's row block m (dZ rows)
+//   K11 unit (i, j)                        needs K10's column tile i (dZ columns)
 // Each epilogue warp of the producing GEMM adds one to its tile's row-block counter
 // and column-tile counter after the tile's TMA stores have completed (release adds);
 // the consumer's TMA producer polls one counter with acquire loads. Every output
@@ -52,6 +55,7 @@
 
 #include <type_traits>
 
+#include "mptp.h"
 #include "mptp_gemm.cuh"
 
 namespace mptp {
@@ -66,11 +70,16 @@ constexpr int CHAIN_BN = 256;
 static_assert(CHAIN_BN == 4 * BK, "a dependency tile is four K blocks");
 constexpr int CHAIN_FWD = 0;         // problem 0: GeLU epilogue (optionally also U), others: store
 constexpr int CHAIN_BWD = 1;         // problem 0: GeLU' epilogue (reads U), others: store
+// Cross-entropy backward, one vocabulary shard: problem 0 (K10) turns recomputed logits into dZ
+// (softmax minus one-hot, times the upstream gradient), problem 1 (K12) accumulates dX across the
+// shards' launches in fp32, problem 2 (K11) stores dE.
+constexpr int CHAIN_CE = 2;
 
 enum ChainDep : int {
     DEP_NONE = 0,
     DEP_ROWS = 1,  // unit (m, n) reads problem 0's row block m (every column tile of it)
     DEP_COLS = 2,  // unit (i, j) reads problem 0's column tile j (every row block of it)
+    DEP_COLS_M = 3,  // unit (i, j) reads problem 0's column tile i (its row block indexes them)
 };
 
 struct ChainProb {
@@ -97,6 +106,15 @@ struct ChainArgs {
     const __nv_bfloat16* aux;  // backward: U (GeLU' operand), row pitch ld_aux
     long long ld_aux;
     int has_out1;             // forward: problem 0 also stores U through its o1 map
+    // cross-entropy backward (CHAIN_CE)
+    const int32_t* target;    // [T] target id of each token
+    const float* lse;         // [T] log-sum-exp of each token's logits (NaN: no gradient)
+    const float* dloss;       // [T] upstream gradient of each token's loss
+    int v_valid;              // vocabulary columns below this are real, the rest padding
+    int col_off;              // first vocabulary column of this launch's shard
+    const float* acc;         // [T, ld_acc] fp32 dX accumulator (read by the last shard)
+    long long ld_acc;
+    int acc_mode;             // ACC_FIRST: store it (o1 map), ACC_MID: add to it, ACC_LAST: read it, store bf16
     uint32_t* status;         // nullable
     unsigned long long budget_ns;
     // Which list positions each pair runs. sched = 0: pair p runs p, p + P, p + 2P, ... (P pairs).
@@ -112,7 +130,7 @@ struct ChainMaps {
     TmapSet m[CHAIN_MAX_PROBS];
 };
 
-template <int NE_>
+template <int NE_, int CHAIN_>
 struct ChainCfg {
     using Base = GemmCfg<CHAIN_BN, EPI_STORE, NE_>;
     static constexpr int NE = NE_;
@@ -123,17 +141,20 @@ struct ChainCfg {
     static constexpr int B_BYTES = Base::B_BYTES;
     static constexpr int STAGE_BYTES = Base::STAGE_BYTES;
     static constexpr uint32_t TMEM_COLS = Base::TMEM_COLS;
-    static constexpr int STG_PER_WARP = STG_BYTES_PER_WARP;
+    // two staging boxes a warp: 32 x 32 bf16 (2 KB), or fp32 (4 KB) where dX is accumulated
+    static constexpr int STG_PER_WARP = CHAIN_ == CHAIN_CE ? 2 * 4096 : STG_BYTES_PER_WARP;
     static constexpr int STG_BYTES = NE * STG_PER_WARP;
     // problem table, list segments, this pair's list positions, TMEM slot and flags words
     static constexpr int EXTRA = CHAIN_MAX_PROBS * 40 + CHAIN_MAX_SEGS * 12 + CHAIN_MAX_PER_PAIR * 2 + 16;
-    // Six stages with either epilogue width (eight warps' staging boxes leave 8 bytes to spare).
+    // Six stages with either epilogue width (eight warps' bf16 staging boxes, or four warps' fp32
+    // boxes, leave 8 bytes to spare).
     static constexpr int STAGES = 6;
     static constexpr int NUM_BARS = 2 * STAGES + 5;
     static constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + STG_BYTES + 8 * NUM_BARS + EXTRA;
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory per block");
     static_assert(STAGES >= 4, "pipeline depth");
     static_assert(NE == 4 || NE == 8, "4 or 8 epilogue warps");
+    static_assert(CHAIN_ != CHAIN_CE || NE == 4, "the cross-entropy chain uses four epilogue warps");
 };
 
 // A problem's fields as the kernel uses them, copied once into shared memory at start-up (the
@@ -168,7 +189,7 @@ __device__ __forceinline__ void chain_dispatch(int prob, F&& f) {
         f(std::integral_constant<int, 0>{});
     } else if (CHAIN == CHAIN_FWD || prob == 1) {
         f(std::integral_constant<int, 1>{});
-    } else if (prob == 2) {
+    } else if (CHAIN == CHAIN_CE || prob == 2) {
         f(std::integral_constant<int, 2>{});
     } else {
         f(std::integral_constant<int, 3>{});
@@ -209,9 +230,9 @@ __device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target,
 }
 
 template <int NE, int CHAIN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ChainCfg<NE>::NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ChainCfg<NE, CHAIN>::NUM_THREADS, 1)
     gemm_chain_kernel(const __grid_constant__ ChainMaps maps, const __grid_constant__ ChainArgs args) {
-    using Cfg = ChainCfg<NE>;
+    using Cfg = ChainCfg<NE, CHAIN>;
     constexpr int STAGES = Cfg::STAGES;
     constexpr int BN = Cfg::BN;
     constexpr int BNH = Cfg::BNH;
@@ -287,11 +308,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ChainCfg<NE>::NUM_TH
     }
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < CHAIN_MAX_PROBS; ++i) {
-            if (i >= 2 && CHAIN == CHAIN_FWD) break;
+            if ((i >= 2 && CHAIN == CHAIN_FWD) || (i >= 3 && CHAIN == CHAIN_CE)) break;
             prefetch_tensormap(&maps.m[i].a);
             prefetch_tensormap(&maps.m[i].b);
             prefetch_tensormap(&maps.m[i].o0);
         }
+        if (CHAIN == CHAIN_CE && args.acc_mode != ACC_LAST) prefetch_tensormap(&maps.m[1].o1);
     }
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, Cfg::TMEM_COLS);
@@ -325,7 +347,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ChainCfg<NE>::NUM_TH
                     const CUtensorMap* tmB = &maps.m[I].b;
                     const int kb_begin = P.pr.kb_begin, kb_end = P.pr.kb_end, a_mn = P.pr.a_mn, b_mn = P.pr.b_mn;
                     // K1, K3 (problem 0) and K5b (problem 3) read only inputs: no dependency code at all.
-                    constexpr bool MAY_DEP = I == 1 || (CHAIN == CHAIN_BWD && I == 2);
+                    constexpr bool MAY_DEP = I == 1 || (CHAIN != CHAIN_FWD && I == 2);
                     const int dep = MAY_DEP ? P.dep : DEP_NONE;
                     const int arow = m_blk * 2 * BM + static_cast<int>(rank) * BM;
                     const int bcol = ncol * BN + static_cast<int>(rank) * BNH;
@@ -334,7 +356,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ChainCfg<NE>::NUM_TH
                     // the pair, so nothing else is added to its K-loop.
                     if (MAY_DEP && dep != DEP_NONE) {
                         const bool rows = dep == DEP_ROWS;
-                        const uint32_t* ctr = rows ? args.row_done + m_blk : args.col_done + ncol;
+                        const uint32_t* ctr = rows ? args.row_done + m_blk
+                                                   : args.col_done + (dep == DEP_COLS_M ? m_blk : ncol);
                         const uint32_t target = WARPS_PER_TILE * static_cast<uint32_t>(rows ? dep_ncols : dep_mblocks);
                         if (!wait_count(ctr, target, ctl)) {
                             ok = false;
@@ -473,6 +496,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ChainCfg<NE>::NUM_TH
                 const int row0 = m_blk * 2 * BM + static_cast<int>(rank) * BM + q * 32;
                 const int row = row0 + lane;
                 const bool row_ok = row < M;
+                // Cross-entropy backward, problem 0: this row's log-sum-exp (log2 units), upstream
+                // gradient and target; a NaN log-sum-exp (invalid target) gives the row no gradient.
+                float lse2 = 0.0f, dl = 0.0f;
+                int tgt = -1;
+                if constexpr (CHAIN == CHAIN_CE && ACT) {
+                    if (row_ok) {
+                        tgt = args.target[row];
+                        lse2 = args.lse[row] * 1.4426950408889634f;
+                        dl = args.dloss[row];
+                        if (!(lse2 == lse2)) {
+                            lse2 = 0.0f;
+                            dl = 0.0f;
+                            tgt = -1;
+                        }
+                    }
+                }
+                // bf16 boxes: with fp32 boxes in the same staging (cross-entropy), box k of either
+                // kind starts at 4 KB k, so a box never overlaps the other one in flight.
+                auto store_bf16 = [&](const uint32_t (&pk)[16], int col0) {
+                    stage_and_store(tmO0, CHAIN == CHAIN_CE ? stg + sbuf * 2048 : stg, sbuf, lane, pk, col0, row0);
+                };
                 auto issue = [&](int cc, uint32_t (&rr)[32], uint32_t (&uu)[16]) {
                     const int c = c_begin + cc;
                     if constexpr (CHAIN == CHAIN_BWD && ACT) {
@@ -519,12 +563,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ChainCfg<NE>::NUM_TH
                                 mul2(make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1])), gp);
                             pk[j] = pack_bf16x2(gv.x, gv.y);
                         }
+                    } else if constexpr (CHAIN == CHAIN_CE && ACT) {
+                        // dZ = dloss (exp(z - lse) - [column == target]), 0 on padding columns.
+                        constexpr float LOG2E = 1.4426950408889634f;
+                        const int gcol0 = args.col_off + col0;
+                        const int lim = args.v_valid - gcol0;
+                        const unsigned dt = static_cast<unsigned>(tgt - gcol0);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            float gz[2];
+#pragma unroll
+                            for (int e2 = 0; e2 < 2; ++e2) {
+                                const int jj = 2 * j + e2;
+                                float pr = ex2_approx(fmaf(__uint_as_float(r[jj]), LOG2E, -lse2));
+                                if (static_cast<int>(dt) == jj && dt < 32u) pr -= 1.0f;
+                                gz[e2] = (jj < lim && dl != 0.0f) ? dl * pr : 0.0f;
+                            }
+                            pk[j] = pack_bf16x2(gz[0], gz[1]);
+                        }
+                    } else if constexpr (CHAIN == CHAIN_CE && I == 1) {
+                        // dX across the shards' launches: the first stores its fp32 tile, the middle
+                        // ones add theirs at L2 (TMA reductions), the last adds the accumulator in
+                        // registers and stores bf16; one addition per shard, in shard order.
+                        if (args.acc_mode != ACC_LAST) {
+                            stage_and_store_f32(&maps.m[1].o1, stg, sbuf, lane, r, col0, row0, args.acc_mode == ACC_MID);
+                            return;
+                        }
+                        float v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+                        if (row_ok) {
+                            const float4* src = reinterpret_cast<const float4*>(args.acc + row * args.ld_acc + col0);
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const float4 a4 = src[j];
+                                v[4 * j] += a4.x;
+                                v[4 * j + 1] += a4.y;
+                                v[4 * j + 2] += a4.z;
+                                v[4 * j + 3] += a4.w;
+                            }
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
                     } else {
 #pragma unroll
                         for (int j = 0; j < 16; ++j)
                             pk[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
                     }
-                    stage_and_store(tmO0, stg, sbuf, lane, pk, col0, row0);
+                    store_bf16(pk, col0);
                 };
                 auto release = [&]() {
                     tc_fence_before();
@@ -599,9 +685,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(ChainCfg<NE>::NUM_TH
     }
 }
 
+// Host side of the list scheduling (mptp_mlp_fused.cu), for the other users of the chain kernel.
+// A problem of M x N outputs over K blocks [kb_begin, kb_end) (operand majorness as ProbInfo),
+// units in groups of `group` row blocks.
+ChainProb chain_problem(int M, int N, int kb_begin, int kb_end, int a_mn, int b_mn, int group);
+// Bytes of zeroed counters a chain over a first problem of M0 x N0 outputs needs (control words,
+// one per 256-row block and per 256-column tile), rounded up to 256.
+size_t chain_counter_bytes(int M0, int N0);
+// One cross-entropy backward shard in one launch: problems 0 (K10), 1 (K12, DEP_ROWS) and 2 (K11,
+// DEP_COLS_M) set up in `a`; `counters` holds chain_counter_bytes of zeros, and is zero again
+// when the launch ends.
+mp_status launch_chain_ce(const ChainMaps& m, ChainArgs& a, int sms, cudaStream_t s, uint32_t* counters);
+
 template <int NE, int CHAIN>
 inline int chain_resident_pairs(int num_sms) {
-    using Cfg = ChainCfg<NE>;
+    using Cfg = ChainCfg<NE, CHAIN>;
     static int cached[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -630,7 +728,7 @@ inline int chain_resident_pairs(int num_sms) {
 // Grid = 2 x `pairs` (the pairs the schedule in args was made for; at most the resident pairs).
 template <int NE, int CHAIN>
 inline cudaError_t launch_gemm_chain(const ChainMaps& maps, const ChainArgs& args, int pairs, cudaStream_t stream) {
-    using Cfg = ChainCfg<NE>;
+    using Cfg = ChainCfg<NE, CHAIN>;
     auto kern = gemm_chain_kernel<NE, CHAIN>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(Cfg::SMEM_BYTES));

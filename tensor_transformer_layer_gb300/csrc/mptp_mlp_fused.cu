@@ -137,6 +137,7 @@ bool list_schedule(const ChainArgs& a, int pairs, Schedule& out) {
             double cur = f.first + SCHED_UNIT;
             if (p.dep == DEP_ROWS) cur = std::max(cur, row_done[static_cast<size_t>(m_blk)] + SCHED_LAT);
             if (p.dep == DEP_COLS) cur = std::max(cur, col_done[static_cast<size_t>(ncol)] + SCHED_LAT);
+            if (p.dep == DEP_COLS_M) cur = std::max(cur, col_done[static_cast<size_t>(m_blk)] + SCHED_LAT);
             cur += L;
             if (sg.prob == 0) {
                 row_done[static_cast<size_t>(m_blk)] = std::max(row_done[static_cast<size_t>(m_blk)], cur + SCHED_EPI);
@@ -247,6 +248,24 @@ mp_status check_workspace(void* ws, size_t bytes, int T, int f) {
 }
 
 }  // namespace
+
+ChainProb chain_problem(int M, int N, int kb_begin, int kb_end, int a_mn, int b_mn, int group) {
+    return chain_prob(M, N, kb_begin, kb_end, a_mn, b_mn, group);
+}
+
+size_t chain_counter_bytes(int M0, int N0) {
+    const size_t words = CHAIN_CTL_WORDS + static_cast<size_t>(ceil_div(M0, 2 * BM)) + ceil_div(N0, CHAIN_BN);
+    return (words * 4 + 255) / 256 * 256;
+}
+
+mp_status launch_chain_ce(const ChainMaps& m, ChainArgs& a, int sms, cudaStream_t s, uint32_t* counters) {
+    a.ctl = counters;
+    a.row_done = counters + CHAIN_CTL_WORDS;
+    a.col_done = a.row_done + a.p[0].pr.num_m_blocks;
+    a.num_counters = a.p[0].pr.num_m_blocks + a.p[0].ncols;
+    return launch_chain_ne<4, CHAIN_CE>(m, a, 3, sms, s);
+}
+
 }  // namespace mptp
 
 using namespace mptp;

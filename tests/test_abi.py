@@ -71,8 +71,12 @@ def test_ce_bwd_workspace_bytes(L):
     import tensor_transformer_layer_gb300 as mp
     a256 = lambda x: (x + 255) // 256 * 256
     T, h, v_pad, t = 8192, 1536, 51200, 8
-    # shard by shard: lse [T] fp32, fp32 dX accumulator [T, h], one shard of dZ [T, v_pad/t] bf16
-    assert mp.mp_vocab_ce_bwd_workspace_bytes(T, h, v_pad, t) == a256(T * 4) + a256(T * h * 4) + a256(T * 6400 * 2)
+    # shard by shard: lse [T] fp32, the chain kernel's counters (64 control words, one per 256-token
+    # row block and per 256-column vocabulary tile of a shard), fp32 dX accumulator [T, h], one shard
+    # of dZ [T, v_pad/t] bf16
+    ctr = a256(4 * (64 + 32 + 25))
+    assert mp.mp_vocab_ce_bwd_workspace_bytes(T, h, v_pad, t) == (a256(T * 4) + ctr + a256(T * h * 4) +
+                                                                 a256(T * 6400 * 2))
     # one pass: lse and every shard's dZ [T, v_pad] bf16
     assert mp.mp_vocab_ce_bwd_workspace_bytes_one_pass(T, h, v_pad, t) == a256(T * 4) + a256(T * v_pad * 2)
     # one shard: the two layouts coincide (no accumulator)

@@ -122,3 +122,50 @@ def test_ce_bwd_invalid_target_contributes_nothing(one_pass):
     assert torch.count_nonzero(dX[7]).item() == 0
     assert rel_fro(f64(dX)[keep], ref["dX"]) <= GRAD_REL_FRO
     assert rel_fro(f64(dE), ref["dE"]) <= GRAD_REL_FRO
+
+
+@pytest.mark.parametrize("T,h,v_pad,v_valid,t", [
+    (300, 128, 2048, 2000, 2),        # two shards: the first stores the accumulator, the last reads it
+    (257, 192, 2048, 1500, 8),        # middle shards add at L2; the last shards hold only padding
+    (1000, 384, 12800, 12345, 4),     # several row blocks and vocabulary tiles a shard
+    (8192, 1536, 51200, 50257, 8),    # the bench workload
+])
+def test_ce_bwd_shard_chain_bitwise_equal_to_separate_launches(T, h, v_pad, v_valid, t, monkeypatch):
+    # Shard by shard, each shard's K10, K12 and K11 run as one launch of the chain kernel. They are
+    # the same tiles and K-loops as the three separate launches (MPTP_CE_BWD_CHAIN=0), with dX
+    # accumulated across shards in the same order, so both gradients are equal bit for bit.
+    inp = synth.ce_inputs(T, h, v_pad, v_valid, seed=8600 + T)
+    dl = _dloss(T, 8601 + T)
+    loss = _forward_loss(inp, v_valid, t)
+    dXc, dEc = _run(inp, dl, v_valid, t, loss=loss)
+    again = _run(inp, dl, v_valid, t, loss=loss)
+    assert torch.equal(dXc, again[0]) and torch.equal(dEc, again[1])
+    monkeypatch.setenv("MPTP_CE_BWD_CHAIN", "0")
+    dXs, dEs = _run(inp, dl, v_valid, t, loss=loss)
+    assert torch.equal(dXc, dXs) and torch.equal(dEc, dEs)
+    if T <= 1000:
+        ref = oracle.ce_bwd(f64(inp["X"]), f64(inp["E"]), inp["target"].numpy(), dl.double().numpy(), v_valid)
+        assert rel_fro(f64(dXc), ref["dX"]) <= GRAD_REL_FRO and rel_fro(f64(dEc), ref["dE"]) <= GRAD_REL_FRO
+
+
+def test_ce_bwd_shard_chain_timeout_reports_and_recovers(monkeypatch):
+    # A zero wait budget: the chain launches give up on their first wait that does not succeed at
+    # once, report MP_DEV_TIMEOUT and return their counters to zero, so the next call is exact.
+    m = mp()
+    T, h, v_pad, v_valid, t = 1000, 384, 12800, 12345, 4
+    inp = synth.ce_inputs(T, h, v_pad, v_valid, seed=8700)
+    dl = _dloss(T, 8701)
+    loss = _forward_loss(inp, v_valid, t)
+    X, E, tgt = inp["X"].cuda(), inp["E"].cuda(), inp["target"].cuda()
+    wsb = torch.empty(m.mp_vocab_ce_bwd_workspace_bytes(T, h, v_pad, t), dtype=torch.uint8, device="cuda")
+    dX = torch.empty(T, h, dtype=torch.bfloat16, device="cuda")
+    dE = torch.empty(v_pad, h, dtype=torch.bfloat16, device="cuda")
+    st = status_tensor()
+    monkeypatch.setenv("MPTP_WAIT_BUDGET_NS", "0")
+    m.mp_vocab_ce_bwd(X, E, tgt, loss, dl.cuda(), dX, dE, wsb, v_valid=v_valid, t=t, d_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & m.MP_DEV_TIMEOUT
+    monkeypatch.delenv("MPTP_WAIT_BUDGET_NS")
+    dX2, dE2 = _run(inp, dl, v_valid, t, loss=loss)
+    ref = oracle.ce_bwd(f64(inp["X"]), f64(inp["E"]), inp["target"].numpy(), dl.double().numpy(), v_valid)
+    assert rel_fro(f64(dX2), ref["dX"]) <= GRAD_REL_FRO and rel_fro(f64(dE2), ref["dE"]) <= GRAD_REL_FRO
