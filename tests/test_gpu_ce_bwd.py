@@ -128,6 +128,7 @@ def test_ce_bwd_invalid_target_contributes_nothing(one_pass):
     (300, 128, 2048, 2000, 2),        # two shards: the first stores the accumulator, the last reads it
     (257, 192, 2048, 1500, 8),        # middle shards add at L2; the last shards hold only padding
     (1000, 384, 12800, 12345, 4),     # several row blocks and vocabulary tiles a shard
+    (200, 64, 1024, 900, 8),          # a shard narrower than one 256-column tile, h = 64
     (8192, 1536, 51200, 50257, 8),    # the bench workload
 ])
 def test_ce_bwd_shard_chain_bitwise_equal_to_separate_launches(T, h, v_pad, v_valid, t, monkeypatch):
