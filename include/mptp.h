@@ -287,7 +287,9 @@ MP_API mp_status mp_vocab_ce_lse(const mp_bf16* X, const mp_bf16* E, const int32
  *   so the same concurrency rule as mp_mlp_fwd_fused applies: run it alone on the
  *   device (beside other kernels it ends with MP_DEV_TIMEOUT rather than hang).
  *   MPTP_CE_BWD_CHAIN=0 in the environment runs each shard as three separate
- *   launches instead, with no such rule; the gradients are the same bit for bit.
+ *   launches instead, with no such rule (so does a shard with more than 4096 output
+ *   tiles, about T > 32k tokens at v_pad / t = 6400); the gradients are the same bit
+ *   for bit.
  *   workspace >= mp_vocab_ce_bwd_workspace_bytes_one_pass(T, h, v_pad, t) bytes
  *   (the log-sum-exp and every shard's dZ, [T, v_pad] bf16: 839 MB at T = 8192,
  *   v_pad = 51,200): dZ of all shards is formed in one launch, then dE and dX in

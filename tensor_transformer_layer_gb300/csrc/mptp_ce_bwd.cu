@@ -17,8 +17,9 @@
 // (mptp_gemm_chain.cuh): a K12 tile starts on a block of tokens once K10 has written
 // that block's dZ rows, a K11 tile once K10 has written its 256 vocabulary columns,
 // so the GEMMs share the SMs instead of each ending in a part-empty wave. The tiles
-// and K-loops are the separate kernels' (MPTP_CE_BWD_CHAIN=0 runs those instead), so
-// the gradients are the same bit for bit. With every shard's dZ in the workspace (one
+// and K-loops are the separate kernels' (MPTP_CE_BWD_CHAIN=0 runs those instead, as does a
+// shard with more tiles than the chain's schedule table holds), so the gradients are the
+// same bit for bit. With every shard's dZ in the workspace (one
 // pass), the three GEMMs run once each over the whole vocabulary.
 // The log-sum-exp comes from the forward: either exported by it (mp_vocab_ce_lse, then
 // mp_vocab_ce_bwd_lse), or rebuilt from its loss: lse = loss + z_target, with z_target
@@ -155,7 +156,13 @@ static mp_status ce_bwd(const mp_bf16* X, const mp_bf16* E, const int32_t* targe
     const double Tb = 2.0 * T, hb = 2.0 * h, vb = 2.0 * vs;
     const unsigned long long budget = wait_budget_ns();
     const char* chain_env = std::getenv("MPTP_CE_BWD_CHAIN");
-    if (C > 1 && !(chain_env && chain_env[0] == '0' && chain_env[1] == '\0')) {
+    const bool chain_off = chain_env && chain_env[0] == '0' && chain_env[1] == '\0';
+    // The chain only where a shard's list fits the precomputed schedule (T up to about 32k tokens
+    // at v_pad / t = 6400): beyond it the chain would take its units round-robin, which leaves
+    // pairs waiting on dependencies that a schedule would have placed after other work.
+    const long long mbT = ceil_div(T, 2 * BM), ncv = ceil_div(vs, CHAIN_BN), nch = ceil_div(h, CHAIN_BN);
+    const long long chain_units = mbT * ncv + mbT * nch + ncv * nch;  // a shard's K10, K12, K11 tiles
+    if (C > 1 && !chain_off && chain_units <= CHAIN_MAX_SCHED) {
         // Each shard's K10, K12 and K11 in one chain launch; its counters start at zero and every
         // launch returns them to zero for the next.
         uint32_t* ctr = reinterpret_cast<uint32_t*>(ws + lay.ctr_off);

@@ -130,6 +130,7 @@ def test_ce_bwd_invalid_target_contributes_nothing(one_pass):
     (1000, 384, 12800, 12345, 4),     # several row blocks and vocabulary tiles a shard
     (200, 64, 1024, 900, 8),          # a shard narrower than one 256-column tile, h = 64
     (8192, 1536, 51200, 50257, 8),    # the bench workload
+    (32512, 1536, 51200, 50257, 8),   # 4092 tiles a shard: the most the chain's schedule table holds
 ])
 def test_ce_bwd_shard_chain_bitwise_equal_to_separate_launches(T, h, v_pad, v_valid, t, monkeypatch):
     # Shard by shard, each shard's K10, K12 and K11 run as one launch of the chain kernel. They are
