@@ -195,6 +195,11 @@ MP_API mp_status mp_mlp_bwd_shards(const mp_bf16* X, const mp_bf16* A, const mp_
  *   Size rules, shard range and outputs as mp_mlp_fwd_shards / mp_mlp_bwd_shards;
  *   dU_ws as mp_mlp_bwd. T = 0: nothing to compute (the backward zeroes its dA and
  *   dB range, as mp_mlp_bwd_shards does) and the workspace is not touched.
+ *   Large layers run as mp_mlp_fwd_shards / mp_mlp_bwd_shards do, as separate
+ *   launches with the same outputs, and leave the workspace untouched: a direction
+ *   with more than 4096 output tiles of 256 x 256 (at h = 3072: the backward beyond
+ *   about 12.5k tokens, the forward beyond about 17k), and any layer with T > 8192
+ *   and h < 2304, where one launch measured 1-7 % slower than the separate ones.
  */
 MP_API size_t mp_mlp_fused_workspace_bytes(int T, int h, int f, int t);
 MP_API mp_status mp_mlp_fwd_fused(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B,

@@ -202,9 +202,11 @@ static mp_status ce_bwd(const mp_bf16* X, const mp_bf16* E, const int32_t* targe
             a.acc_mode = i == 0 ? ACC_FIRST : (i == C - 1 ? ACC_LAST : ACC_MID);
             a.status = d_status;
             a.budget_ns = budget;
-            if ((st = launch_chain_ce(m, a, sms, s, ctr)) != MP_OK) return st;
+            st = launch_chain_ce(m, a, sms, s, ctr);
+            if (st == CHAIN_NO_SCHEDULE && i == 0) break;  // no schedule: the separate launches below
+            if (st != MP_OK) return st;
         }
-        return MP_OK;
+        if (st == MP_OK) return MP_OK;
     }
     for (int i = 0; i < C; ++i) {
         const __nv_bfloat16* Ei = Eb + static_cast<long long>(i) * vs * h;

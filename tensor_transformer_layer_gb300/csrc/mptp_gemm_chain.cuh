@@ -694,8 +694,15 @@ ChainProb chain_problem(int M, int N, int kb_begin, int kb_end, int a_mn, int b_
 size_t chain_counter_bytes(int M0, int N0);
 // One cross-entropy backward shard in one launch: problems 0 (K10), 1 (K12, DEP_ROWS) and 2 (K11,
 // DEP_COLS_M) set up in `a`; `counters` holds chain_counter_bytes of zeros, and is zero again
-// when the launch ends.
+// when the launch ends. CHAIN_NO_SCHEDULE (nothing launched) when the list does not fit the
+// schedule tables.
 mp_status launch_chain_ce(const ChainMaps& m, ChainArgs& a, int sms, cudaStream_t s, uint32_t* counters);
+// Returned by the host side when a list has no precomputed schedule (more positions than
+// CHAIN_MAX_SCHED, or a pair's share beyond CHAIN_MAX_PER_PAIR); the callers then run the same
+// GEMMs as separate launches. (The kernel's round-robin order, which needs no tables, leaves pairs
+// waiting on dependencies that a schedule places after other work: measured 20-40 % slower than the
+// separate launches at T = 16384 and 32768.)
+constexpr mp_status CHAIN_NO_SCHEDULE = static_cast<mp_status>(-1);
 
 template <int NE, int CHAIN>
 inline int chain_resident_pairs(int num_sms) {

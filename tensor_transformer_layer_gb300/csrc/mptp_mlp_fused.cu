@@ -88,6 +88,12 @@ int min_row_group(int m_blocks) { return ceil_div(m_blocks, (CHAIN_MAX_SEGS - 4)
 // h <= 2048: equal or up to 2 % faster with eight (8192 x 1536); at h = 3072 four are 1 % faster.
 bool chain_ne8(int h) { return h <= 2048; }
 
+// Where one launch measured no slower than the separate launches (CUDA events, same box): every
+// width at T <= 8192 (1-10 % faster over the layer sweep), and h >= 2304 at T = 16384 (forward 1-4 %,
+// backward 6 % faster). At T = 16384 with h <= 1920 and T = 32768 with h = 1536 the one-launch
+// forward was 2-7 % slower and the backward about 1 %; those layers run the separate launches.
+bool chain_pays(int T, int h) { return T <= 8192 || h >= 2304; }
+
 // Host copy of the kernel's position decode (chain_decode).
 void decode_host(const ChainProb& p, int lu, int& m_blk, int& ncol) {
     const int per_group = p.group * p.ncols;
@@ -233,6 +239,7 @@ template <int NE, int CHAIN>
 mp_status launch_chain_ne(const ChainMaps& m, ChainArgs& a, int nprobs, int sms, cudaStream_t s) {
     const int pairs = chain_pairs<NE, CHAIN>(sms, nprobs, a);
     if (!plan_chain(a, nprobs, pairs)) return MP_ERR_UNSUPPORTED_SHAPE;
+    if (!a.sched) return CHAIN_NO_SCHEDULE;
     return launch_gemm_chain<NE, CHAIN>(m, a, pairs, s) == cudaSuccess ? MP_OK : MP_ERR_CUDA;
 }
 
@@ -288,6 +295,8 @@ extern "C" mp_status mp_mlp_fwd_fused(const mp_bf16* X, const mp_bf16* A, const 
     if ((st = check_workspace(workspace, workspace_bytes, T, f)) != MP_OK) return st;
     int sms = 0;
     if ((st = check_device(&sms)) != MP_OK) return st;
+    if (!chain_pays(T, h))
+        return mp_mlp_fwd_shards(X, A, B, Z, Y, U_save, T, h, f, t, shard_begin, shard_count, d_status, stream);
     const int fs = f / t;
     const int c0 = shard_begin * fs, nc = shard_count * fs;
 
@@ -316,7 +325,10 @@ extern "C" mp_status mp_mlp_fwd_fused(const mp_bf16* X, const mp_bf16* A, const 
     a.has_out1 = U_save ? 1 : 0;
     a.status = d_status;
     a.budget_ns = wait_budget_ns();
-    return launch_chain<CHAIN_FWD>(m, a, 2, sms, static_cast<cudaStream_t>(stream), h);
+    st = launch_chain<CHAIN_FWD>(m, a, 2, sms, static_cast<cudaStream_t>(stream), h);
+    if (st == CHAIN_NO_SCHEDULE)  // too many tiles for the schedule tables: the separate launches
+        return mp_mlp_fwd_shards(X, A, B, Z, Y, U_save, T, h, f, t, shard_begin, shard_count, d_status, stream);
+    return st;
 }
 
 extern "C" mp_status mp_mlp_bwd_fused(const mp_bf16* X, const mp_bf16* A, const mp_bf16* B, const mp_bf16* U,
@@ -345,6 +357,9 @@ extern "C" mp_status mp_mlp_bwd_fused(const mp_bf16* X, const mp_bf16* A, const 
         return MP_OK;
     }
 
+    if (!chain_pays(T, h))
+        return mp_mlp_bwd_shards(X, A, B, U, Y, dZ, dX, dA, dB, dU_ws, T, h, f, t, shard_begin, shard_count, d_status,
+                                 stream);
     ChainMaps m{};
     ChainArgs a{};
     // K3: dU_r = (dZ B_r^T) * GeLU'(U_r); both operands K-major.
@@ -383,5 +398,9 @@ extern "C" mp_status mp_mlp_bwd_fused(const mp_bf16* X, const mp_bf16* A, const 
     a.ld_aux = f;
     a.status = d_status;
     a.budget_ns = wait_budget_ns();
-    return launch_chain<CHAIN_BWD>(m, a, 4, sms, s, h);
+    st = launch_chain<CHAIN_BWD>(m, a, 4, sms, s, h);
+    if (st == CHAIN_NO_SCHEDULE)  // too many tiles for the schedule tables: the separate launches
+        return mp_mlp_bwd_shards(X, A, B, U, Y, dZ, dX, dA, dB, dU_ws, T, h, f, t, shard_begin, shard_count, d_status,
+                                 stream);
+    return st;
 }
