@@ -9,8 +9,9 @@
 // finished. At small layers (T = 2048 tokens, h = 1536: 20-26 us of MMA work a
 // GEMM) that costs 7-10 us a launch. Here the units of all GEMMs of a direction
 // form one list in a fixed order. The host gives each CTA pair its positions in the
-// list (a greedy list-scheduling pass over the pairs, cached per shape; failing that,
-// pair p takes positions p, p + P, p + 2P, ...). A unit that reads another GEMM's output
+// list (a greedy list-scheduling pass over the pairs, cached per shape; a list too long
+// for the tables runs as separate launches instead, although the kernel can also take
+// positions round-robin, pair p taking p, p + P, p + 2P, ...). A unit that reads another GEMM's output
 // waits, once before its first load, for the part of it that it reads:
 //   K2 unit (row block m, column tile n)   needs K1's row block m
 //   K4 unit (m, n)                         needs K3's row block m

@@ -118,8 +118,8 @@ struct Schedule {
 // Greedy list scheduling of the list over `pairs` CTA pairs: each position, in order, goes to the
 // pair that is free first (the lowest index among equals); a unit that reads problem 0's output
 // starts once the row block or column tile it reads is complete. Each pair's positions come out
-// increasing. Returns false when the schedule would not fit the kernel's tables (the round-robin
-// order is used then).
+// increasing. Returns false when the schedule would not fit the kernel's tables (the callers then
+// run the separate launches).
 bool list_schedule(const ChainArgs& a, int pairs, Schedule& out) {
     out.makespan = 0.0;
     if (a.total_units > CHAIN_MAX_SCHED || pairs > CHAIN_MAX_PAIRS || pairs < 1) return false;
@@ -169,11 +169,11 @@ bool list_schedule(const ChainArgs& a, int pairs, Schedule& out) {
 // (problem 1's group g after problem 0's group g + lag); every (G, lag) with G a power of two up to
 // the row blocks and lag up to 3 is scheduled by the list-scheduling pass and the shortest
 // simulated makespan is kept (the first of equals). Cached by the problems' geometry and the pair
-// count. If no schedule fits the kernel's tables, groups of min_row_group rows, lag 0 and the
-// round-robin order.
+// count. If no schedule fits the kernel's tables, groups of min_row_group rows, lag 0 and no
+// schedule (launch_chain_ne then answers CHAIN_NO_SCHEDULE).
 struct Plan {
     int group = 1, lag = 0;
-    Schedule sched;  // empty: round-robin
+    Schedule sched;  // empty: none fits the tables
 };
 
 bool plan_chain(ChainArgs& a, int nprobs, int pairs) {
